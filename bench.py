@@ -1,0 +1,431 @@
+"""Benchmark of the sparse MLA hot path (forward + backward) on GB300.
+
+One step = sparse_mla_fwd then sparse_mla_bwd (Delta pass, dKV zeroing, main
+backward kernel, dKV cast) over the headline workload: T=65536 packed tokens,
+H=128, topk=2048, ragged log-uniform sequence lengths in [128, 32768],
+q ~ N(0, 8^2), 1% all-padding rows.  Inputs are seeded synthetic data resident
+in HBM when the timed region starts; L2 is flushed (a 256 MiB write) before
+every timed step, outside the step's CUDA events.
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead,
+on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bwd_sparse_mla_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse-MLA fwd+bwd tokens/s at H=128, topk=2048 (T=65536)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GATHER_BYTES_PER_SLOT = 1152          # one 576-wide bf16 KV row per valid slot
+FWD_FLOP_PER_SLOT_HEAD = 2 * 1088     # QK^T over 576 + PV over 512
+BWD_FLOP_PER_SLOT_HEAD = 2 * 2752     # S 576 + dP 512 + dQ 576 + dKV 512+576
+DKV_RED_BYTES_PER_SLOT = 2304         # fp32 scatter of a 576-wide row
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = x
+            walk(d)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                for k, v in flat.items():
+                    if k.split(".")[-1] == key and isinstance(v, (int, float)):
+                        out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None, log_path: str | None):
+        self.proc = None
+        self.log_path = log_path
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        if self.log_path:
+            try:
+                with open(self.log_path, "w") as f:
+                    f.write(self.FIELDS + "\n" + out)
+            except Exception:
+                pass
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def bus_id_of(dev) -> str | None:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return None
+
+
+def oracle_tokens_per_s(w, target_s: float, seed: int = 17):
+    """Time the fp64 oracle (forward then backward) on a bounded row sample."""
+    import oracle.sparse_mla_ref as orc
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.T, size=2, replace=False))
+    t0 = time.perf_counter()
+    o, l = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, rows=rows)
+    orc.sparse_mla_bwd(w.q, w.kv, o, w.dout, l, w.indices, w.scale, rows=rows)
+    per_row = (time.perf_counter() - t0) / rows.size
+    n = int(max(2, min(w.T, target_s / max(per_row, 1e-6))))
+    rows = np.sort(rng.choice(w.T, size=n, replace=False))
+    t0 = time.perf_counter()
+    o, l = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, rows=rows)
+    orc.sparse_mla_bwd(w.q, w.kv, o, w.dout, l, w.indices, w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        th = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if th:
+            return int(max(th))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.make_workload(args.config, values=False)
+    rng = np.random.default_rng(99)
+    n_rows = args.ref_rows
+    samples = [np.sort(rng.choice(w.T, size=n_rows, replace=False)) for _ in range(args.warmup + args.steps)]
+    W.draw_values(w, rows=np.concatenate(samples))
+    import oracle.sparse_mla_ref as orc
+    times = []
+    for i, rows in enumerate(samples):
+        t0 = time.perf_counter()
+        o, l = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, rows=rows)
+        orc.sparse_mla_bwd(w.q, w.kv, o, w.dout, l, w.indices, w.scale, rows=rows)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step_s = float(np.mean(times))
+    value = n_rows / step_s
+    cores = blas_threads()
+    sample = f"{n_rows} random rows of the {w.name} workload per step (fwd+bwd, fp64)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "topk": w.topk, "rows_per_step": n_rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from bwd_sparse_mla_gb300 import capi
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    capi.load()
+
+    w = W.make_workload(args.config)
+    n_valid = w.n_valid()
+    T, H, topk = w.T, w.H, w.topk
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    h_q, h_kv, h_dout = bf(w.q), bf(w.kv), bf(w.dout)
+    h_idx = torch.from_numpy(np.ascontiguousarray(w.indices))
+    h_cu = torch.from_numpy(w.cu_seqlens)
+    q, kv, dout = h_q.to(dev), h_kv.to(dev), h_dout.to(dev)
+    idx, cu = h_idx.to(dev), h_cu.to(dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dq = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    dkv32 = torch.empty((T, 1, 576), dtype=torch.float32, device=dev)
+    dkv = torch.empty((T, 1, 576), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk), 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        capi.sparse_mla_fwd(q, kv, idx, cu, w.scale, out=out, lse=lse)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dq=dq, dkv_f32=dkv32, dkv=dkv,
+                            workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    log_dir = os.path.join(ROOT, "gpurun_out")
+    sampler = ClockSampler(bus_id_of(dev), os.path.join(log_dir, "clocks.csv") if os.path.isdir(log_dir) else None)
+    launches0 = capi.sparse_mla_launch_count()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        capi.sparse_mla_fwd(q, kv, idx, cu, w.scale, out=out, lse=lse)
+        ev[k][1].record(stream)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dq=dq, dkv_f32=dkv32, dkv=dkv,
+                            workspace=ws)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    launches = capi.sparse_mla_launch_count() - launches0
+    clocks = sampler.stop()
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    ms = fwd_ms + bwd_ms
+    if world > 1:
+        t = torch.tensor([ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, fwd_ms, bwd_ms = [float(x) for x in t.tolist()]
+    value = world * T / (ms / 1e3)
+
+    # finite-output check of the last timed step (outside the timed region)
+    finite = bool(torch.isfinite(lse).all()) and bool(torch.isfinite(dkv32).all())
+
+    peaks, peak_src = load_peaks()
+    fwd_flop = FWD_FLOP_PER_SLOT_HEAD * H * n_valid
+    bwd_flop = BWD_FLOP_PER_SLOT_HEAD * H * n_valid
+    gbytes = GATHER_BYTES_PER_SLOT * n_valid
+    tflops_peak = peaks["bf16_tflops_sustained"]
+    hbm = peaks["hbm_gbs"]
+
+    def bound_ms(flop):
+        return max(flop / (tflops_peak * 1e12), gbytes / (hbm * 1e9)) * 1e3
+
+    ridge = tflops_peak * 1e12 / (hbm * 1e9)
+    bwd_tensor = bwd_flop / gbytes > ridge
+    if bwd_tensor:
+        achieved = bwd_flop / (bwd_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
+                "frac": achieved / tflops_peak}
+    else:
+        achieved = gbytes / (bwd_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+    roof.update({
+        "kernel": "sparse_mla_bwd call (Delta + dKV zero + main backward + dKV cast)",
+        "peak_source": f"{peak_src} bf16_tflops_sustained / hbm_gbs",
+        "algorithmic_per_launch": {"flop": bwd_flop, "gathered_kv_bytes": gbytes},
+        "traffic": None,
+    })
+    tr = traffic_record()
+    if tr is not None:
+        roof["traffic"] = tr["dram_bytes_per_launch"]
+        roof["traffic_note"] = tr["note"]
+
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu)
+        if world > 1:
+            t = torch.tensor([e2e["ms_per_step"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = float(t.item())
+            e2e["value"] = world * T / (e2e["ms_per_step"] / 1e3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = oracle_tokens_per_s(w, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} random rows of the workload, fwd+bwd in fp64 ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "T": T, "H": H, "topk": topk, "valid_slots": n_valid,
+                       "sequences": w.B, "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single-gpu"},
+            "fwd": {"ms": fwd_ms, "tflops": fwd_flop / (fwd_ms * 1e-3) / 1e12,
+                    "roofline_frac": bound_ms(fwd_flop) / fwd_ms},
+            "bwd": {"ms": bwd_ms, "tflops": bwd_flop / (bwd_ms * 1e-3) / 1e12,
+                    "roofline_frac": bound_ms(bwd_flop) / bwd_ms,
+                    "dkv_scatter_bytes": DKV_RED_BYTES_PER_SLOT * n_valid},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": launches,
+            "wall_s_timed": wall,
+            "outputs_finite": finite,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def traffic_record():
+    """Per-launch DRAM traffic of the backward call from a committed ncu
+    summary, used only if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+        if rec.get("source_hash") != kernel_source_hash():
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bwd_sparse_mla_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
+    """Same step through the public API from pinned host buffers: H2D of the
+    inputs, forward, backward, D2H of out, lse, dq and dkv (bf16)."""
+    import torch
+    T, H = w.T, w.H
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    hq, hkv, hdo, hidx, hcu = pin(h_q), pin(h_kv), pin(h_dout), pin(h_idx), pin(h_cu)
+    o_out = torch.empty((T, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    o_lse = torch.empty((T, H), dtype=torch.float32, pin_memory=True)
+    o_dq = torch.empty((T, H, 576), dtype=torch.bfloat16, pin_memory=True)
+    o_dkv = torch.empty((T, 1, 576), dtype=torch.bfloat16, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hkv, hdo, hidx, hcu))
+    d2h = sum(t.numel() * t.element_size() for t in (o_out, o_lse, o_dq, o_dkv))
+    stream = torch.cuda.current_stream()
+
+    def one():
+        q = hq.to(dev, non_blocking=True)
+        kv = hkv.to(dev, non_blocking=True)
+        do = hdo.to(dev, non_blocking=True)
+        idx = hidx.to(dev, non_blocking=True)
+        cu = hcu.to(dev, non_blocking=True)
+        out, lse = capi.sparse_mla_fwd(q, kv, idx, cu, w.scale)
+        dq, _, dkv = capi.sparse_mla_bwd(q, kv, out, do, lse, idx, cu, w.scale)
+        o_out.copy_(out, non_blocking=True)
+        o_lse.copy_(lse, non_blocking=True)
+        o_dq.copy_(dq, non_blocking=True)
+        o_dkv.copy_(dkv, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, args.e2e_steps))
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.mean(times))
+    return {"value": T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, help="workload 1..5 (5 = headline)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,139 @@
+"""Thin ctypes binding of libsparse_mla.so (argument marshalling only).
+
+Function names match the C ABI in include/sparse_mla.h.  Tensors are torch
+CUDA tensors (PyTorch supplies device memory and streams); every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or the call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsparse_mla.so")
+
+SMLA_DKV_ATOMIC = 0
+SMLA_DKV_DETERMINISTIC = 1
+D_QK = 576
+D_V = 512
+
+_lib = None
+
+
+class SparseMLAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"sparse_mla error {code}: {msg}")
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with bwd_sparse_mla_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, F, P, P, P]
+    lib.sparse_mla_fwd.restype = I
+    lib.sparse_mla_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    lib.sparse_mla_bwd_workspace_bytes.restype = S
+    lib.sparse_mla_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, P, P, P, P, S, P]
+    lib.sparse_mla_bwd.restype = I
+    lib.sparse_mla_check_indices.argtypes = [P, I, I, P, I, ctypes.POINTER(ctypes.c_int64), P]
+    lib.sparse_mla_check_indices.restype = I
+    lib.sparse_mla_last_error.argtypes = []
+    lib.sparse_mla_last_error.restype = ctypes.c_char_p
+    lib.sparse_mla_version.argtypes = []
+    lib.sparse_mla_version.restype = ctypes.c_char_p
+    lib.sparse_mla_launch_count.argtypes = []
+    lib.sparse_mla_launch_count.restype = ctypes.c_uint64
+    _lib = lib
+    return lib
+
+
+def sparse_mla_last_error() -> str:
+    return load().sparse_mla_last_error().decode()
+
+
+def sparse_mla_version() -> str:
+    return load().sparse_mla_version().decode()
+
+
+def sparse_mla_launch_count() -> int:
+    return int(load().sparse_mla_launch_count())
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise SparseMLAError(rc, sparse_mla_last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dims(q, indices):
+    T, H, dq = q.shape
+    assert dq == D_QK, "q must be [T, H, 576]"
+    topk = indices.shape[-1]
+    return T, H, topk
+
+
+def sparse_mla_fwd(q, kv, indices, cu_seqlens, scale, out=None, lse=None, stream=None):
+    """out [T,H,512] bf16, lse [T,H] fp32 = forward of q [T,H,576] bf16,
+    kv [T,1,576] bf16, indices [T,1,topk] int32 (-1 = padding)."""
+    T, H, topk = _dims(q, indices)
+    if out is None:
+        out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(load().sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(cu_seqlens), T, H, topk, B,
+                                 float(scale), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def sparse_mla_bwd_workspace_bytes(T: int, H: int, topk: int, dkv_mode: int = SMLA_DKV_ATOMIC) -> int:
+    return int(load().sparse_mla_bwd_workspace_bytes(T, H, topk, dkv_mode))
+
+
+def sparse_mla_bwd(q, kv, out, dout, lse, indices, cu_seqlens, scale, dkv_mode=SMLA_DKV_ATOMIC,
+                   dq=None, dkv_f32=None, dkv=None, workspace=None, want_bf16_dkv=True, stream=None):
+    """dq [T,H,576] bf16, dkv_f32 [T,1,576] fp32 and (optionally) dkv bf16."""
+    T, H, topk = _dims(q, indices)
+    dev = q.device
+    if dq is None:
+        dq = torch.empty((T, H, D_QK), dtype=torch.bfloat16, device=dev)
+    if dkv_f32 is None:
+        dkv_f32 = torch.empty((T, 1, D_QK), dtype=torch.float32, device=dev)
+    if dkv is None and want_bf16_dkv:
+        dkv = torch.empty((T, 1, D_QK), dtype=torch.bfloat16, device=dev)
+    need = sparse_mla_bwd_workspace_bytes(T, H, topk, dkv_mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(load().sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(out), _ptr(dout), _ptr(lse), _ptr(indices),
+                                 _ptr(cu_seqlens), T, H, topk, B, float(scale), int(dkv_mode), _ptr(dq),
+                                 _ptr(dkv_f32), _ptr(dkv), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)))
+    return dq, dkv_f32, dkv
+
+
+def sparse_mla_check_indices(indices, cu_seqlens, stream=None) -> int:
+    T = indices.shape[0]
+    topk = indices.shape[-1]
+    B = cu_seqlens.numel() - 1
+    n_bad = ctypes.c_int64(0)
+    _check(load().sparse_mla_check_indices(_ptr(indices), T, topk, _ptr(cu_seqlens), B,
+                                           ctypes.byref(n_bad), _stream(stream)))
+    return int(n_bad.value)

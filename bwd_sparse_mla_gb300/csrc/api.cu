@@ -1,0 +1,187 @@
+// C ABI of the sparse MLA library: argument validation, device checks and
+// the launch sequence of each call.  Declarations and the contract of every
+// entry point are in include/sparse_mla.h.
+#include <errno.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <cmath>
+#include <string>
+
+#include "../../include/sparse_mla.h"
+#include "smla_common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(-EIO, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_h(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
+
+// The kernels are built for sm_103a only; refuse any other device.
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(-ENOTSUP, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                major, minor);
+  return 0;
+}
+
+int check_shape(int T, int H, int topk, float scale) {
+  if (T < 0) return fail(-EINVAL, "T must be >= 0 (got %d)", T);
+  if (!supported_h(H)) return fail(-EINVAL, "H must be one of 8, 16, 32, 64, 128 (got %d)", H);
+  if (topk <= 0 || topk % 64 != 0)
+    return fail(-EINVAL, "topk must be a positive multiple of 64 (got %d)", topk);
+  if (!std::isfinite(scale)) return fail(-EINVAL, "scale must be finite");
+  return 0;
+}
+
+#define SMLA_REQUIRE_PTR(p)                                                   \
+  do {                                                                        \
+    if ((p) == nullptr) return fail(-EINVAL, "%s must not be NULL", #p);      \
+    if (!aligned16(p)) return fail(-EINVAL, "%s must be 16-byte aligned", #p); \
+  } while (0)
+
+size_t delta_bytes(int T, int H) { return (((size_t)T * H * sizeof(float)) + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sparse_mla_last_error(void) { return g_last_error.c_str(); }
+
+const char* sparse_mla_version(void) { return "sparse_mla_gb300 0.1.0 (sm_103a)"; }
+
+uint64_t sparse_mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
+                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                   smla_bf16_t* out, float* lse, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  if (T == 0) return 0;
+  SMLA_REQUIRE_PTR(q);
+  SMLA_REQUIRE_PTR(kv);
+  SMLA_REQUIRE_PTR(indices);
+  SMLA_REQUIRE_PTR(out);
+  SMLA_REQUIRE_PTR(lse);
+  if (int r = check_device()) return r;
+  smla::FwdArgs a{q, kv, indices, out, lse, T, H, topk, scale};
+  cudaError_t e = smla::launch_fwd_simt(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_fwd launch");
+  count_launches(1);
+  return 0;
+}
+
+size_t sparse_mla_bwd_workspace_bytes(int T, int H, int topk, int dkv_mode) {
+  if (T < 0 || !supported_h(H) || topk <= 0 || topk % 64 != 0) return 0;
+  if (dkv_mode != SMLA_DKV_ATOMIC) return 0;
+  return delta_bytes(T, H);
+}
+
+int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                   const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                   int dkv_mode, smla_bf16_t* dq, float* dkv_f32, smla_bf16_t* dkv,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  if (dkv_mode == SMLA_DKV_DETERMINISTIC)
+    return fail(-ENOTSUP, "dkv_mode SMLA_DKV_DETERMINISTIC is not built");
+  if (dkv_mode != SMLA_DKV_ATOMIC) return fail(-EINVAL, "unknown dkv_mode %d", dkv_mode);
+  if (T == 0) return 0;
+  SMLA_REQUIRE_PTR(q);
+  SMLA_REQUIRE_PTR(kv);
+  SMLA_REQUIRE_PTR(out);
+  SMLA_REQUIRE_PTR(dout);
+  SMLA_REQUIRE_PTR(lse);
+  SMLA_REQUIRE_PTR(indices);
+  SMLA_REQUIRE_PTR(dq);
+  SMLA_REQUIRE_PTR(dkv_f32);
+  if (dkv != nullptr && !aligned16(dkv)) return fail(-EINVAL, "dkv must be 16-byte aligned");
+  SMLA_REQUIRE_PTR(workspace);
+  const size_t need = delta_bytes(T, H);
+  if (workspace_bytes < need)
+    return fail(-EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (int r = check_device()) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  cudaError_t e = smla::launch_delta(out, dout, delta, (int64_t)T * H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "delta launch");
+  count_launches(1);
+  e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
+  smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
+  e = smla::launch_bwd_simt(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
+  count_launches(1);
+  if (dkv != nullptr) {
+    e = smla::launch_cast_bf16(dkv_f32, dkv, (int64_t)T * smla::kDqk, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dkv cast launch");
+    count_launches(1);
+  }
+  return 0;
+}
+
+int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
+                             int B, int64_t* n_bad, void* stream) {
+  g_last_error.clear();
+  if (n_bad == nullptr) return fail(-EINVAL, "n_bad must not be NULL");
+  *n_bad = 0;
+  if (T < 0) return fail(-EINVAL, "T must be >= 0 (got %d)", T);
+  if (topk <= 0) return fail(-EINVAL, "topk must be positive (got %d)", topk);
+  if (B < 1) return fail(-EINVAL, "B must be >= 1 (got %d)", B);
+  if (T == 0) return 0;
+  SMLA_REQUIRE_PTR(indices);
+  if (cu_seqlens == nullptr) return fail(-EINVAL, "cu_seqlens must not be NULL");
+  if (int r = check_device()) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* counter = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&counter), sizeof(*counter), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+  unsigned long long host = 0;
+  e = cudaMemsetAsync(counter, 0, sizeof(*counter), s);
+  if (e == cudaSuccess) {
+    e = smla::launch_check_indices(indices, T, topk, cu_seqlens, B, counter, s);
+    if (e == cudaSuccess) count_launches(1);
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, counter, sizeof(host), cudaMemcpyDeviceToHost, s);
+  cudaError_t e2 = cudaFreeAsync(counter, s);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_check_indices");
+  *n_bad = (int64_t)host;
+  return 0;
+}
+
+}  // extern "C"

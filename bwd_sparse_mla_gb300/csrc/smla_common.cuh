@@ -1,0 +1,82 @@
+// Shared device helpers and launch-argument structs of the sparse MLA library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smla {
+
+constexpr int kDqk = 576;    // 512 latent + 64 rope tail
+constexpr int kDv = 512;     // latent = value width
+constexpr int kDtail = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// ln(1e-30): the LSE of a row with no valid slot (empty max read as 0,
+// sum of exponentials floored at 1e-30).
+constexpr float kLseEmpty = -69.07755278982137f;
+constexpr float kSumexpFloor = 1e-30f;
+
+struct FwdArgs {
+  const uint16_t* q;        // [T, H, 576] bf16
+  const uint16_t* kv;       // [T, 576] bf16
+  const int32_t* indices;   // [T, topk]
+  uint16_t* out;            // [T, H, 512] bf16
+  float* lse;               // [T, H]
+  int T, H, topk;
+  float scale;
+};
+
+struct BwdArgs {
+  const uint16_t* q;
+  const uint16_t* kv;
+  const uint16_t* dout;     // [T, H, 512] bf16
+  const float* lse;         // [T, H]
+  const float* delta;       // [T, H] (workspace, filled by the Delta pass)
+  const int32_t* indices;
+  uint16_t* dq;             // [T, H, 576] bf16
+  float* dkv32;             // [T, 576] fp32 accumulator (zeroed before)
+  int T, H, topk;
+  float scale;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (inputs here are finite).
+__device__ __forceinline__ uint32_t f2bf(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f2bf(lo) | (f2bf(hi) << 16);
+}
+
+// 16-byte vector fp32 reduction into global memory (sm_90+).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Host-side launchers implemented in the kernel translation units.
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t rows,
+                         cudaStream_t s);
+cudaError_t launch_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t s);
+cudaError_t launch_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
+                                 int B, unsigned long long* counter, cudaStream_t s);
+
+}  // namespace smla

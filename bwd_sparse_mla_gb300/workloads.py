@@ -75,8 +75,12 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return r.astype(np.uint16)
 
 
-def _normal_bf16(seed: int, stream: int, shape: tuple, std: float, threads: int) -> np.ndarray:
-    """Draw N(0, std^2) in fp32, round to bf16 bits; chunked over the first axis."""
+def _normal_bf16(seed: int, stream: int, shape: tuple, std: float, threads: int,
+                 rows=None) -> np.ndarray:
+    """Draw N(0, std^2) in fp32, round to bf16 bits; chunked over the first axis.
+
+    With `rows`, only the chunks holding those rows are drawn (the others are
+    left unset); every drawn value is identical to a full draw."""
     T = shape[0]
     row = int(np.prod(shape[1:])) if len(shape) > 1 else 1
     out = np.empty((T, row), dtype=np.uint16)
@@ -92,12 +96,13 @@ def _normal_bf16(seed: int, stream: int, shape: tuple, std: float, threads: int)
             x *= np.float32(std)
         out[lo:hi] = f32_to_bf16_bits(x)
 
-    if n_chunks <= 1 or threads <= 1:
-        for c in range(n_chunks):
+    chunks = range(n_chunks) if rows is None else sorted({int(r) // _CHUNK_TOKENS for r in rows if 0 <= r < T})
+    if len(chunks) <= 1 or threads <= 1:
+        for c in chunks:
             fill(c)
     else:
         with ThreadPoolExecutor(max_workers=threads) as ex:
-            list(ex.map(fill, range(n_chunks)))
+            list(ex.map(fill, chunks))
     return out.reshape(shape)
 
 
@@ -191,12 +196,14 @@ def make_workload(config: int, seed: int | None = None, threads: int | None = No
     return w
 
 
-def draw_values(w: Workload, threads: int | None = None) -> None:
+def draw_values(w: Workload, threads: int | None = None, rows=None) -> None:
+    """Draw q, kv and dO.  With `rows`, q and dO are drawn only for the chunks
+    holding those tokens (kv is always drawn in full)."""
     if threads is None:
         threads = min(32, os.cpu_count() or 1)
-    w.q = _normal_bf16(w.seed, 1, (w.T, w.H, D_QK), w.q_std, threads)
+    w.q = _normal_bf16(w.seed, 1, (w.T, w.H, D_QK), w.q_std, threads, rows)
     w.kv = _normal_bf16(w.seed, 2, (w.T, 1, D_QK), 1.0, threads)
-    w.dout = _normal_bf16(w.seed, 3, (w.T, w.H, D_LATENT), 1.0, threads)
+    w.dout = _normal_bf16(w.seed, 3, (w.T, w.H, D_LATENT), 1.0, threads, rows)
 
 
 def make_custom(T: int, H: int, topk: int, seqlens: list, seed: int, kind: str = "causal",

@@ -1,0 +1,143 @@
+/*
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse MLA attention library.
+ *
+ * DSA-style sparse MLA attention: each query token t has H heads; all heads
+ * attend to the same top-k rows of one latent KV tensor (a single KV group),
+ * named by an int32 index tensor in which -1 marks an unused slot.  A KV row
+ * has 576 elements: a 512-wide latent part, which is also the value V, and a
+ * 64-wide rope tail, which is only part of the key K.
+ *
+ * Sources (web pages, cited by title and section):
+ *   slime issue #2201 "GLM-5.2 SparseMLA TileLang backward returns NaN
+ *     gradients from finite inputs" -- "Strongest repro evidence" gives the
+ *     backward call sparse_mla_bwd(q, kv, tl_out, grad_output, indices,
+ *     tl_lse, sm_scale) and the outputs tl_dq / tl_dkv; "Suspected area" the
+ *     D = 512 latent width and the atomic dKV accumulation.
+ *   miles PR #2079 summary "fix -1 index OOB and NaN gradients in the GLM-5
+ *     sparse-MLA kernel" -- implementation breakdown items 1-3 and the key
+ *     code fragments of the forward `main` and `sparse_mla_bwd_kernel`:
+ *     clamp + mask of -1 slots to exact-zero K/V, the 1e-30 floor on the sum
+ *     of exponentials, and the clamped (no-op) dKV atomic add.
+ *   Megatron-Bridge PR #17 "GLM-5 DSA option: tilelang (2/2)" -- Summary and
+ *     Bug fixes: packed thd layout, top-k padded to a fixed width with -1.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     (row-major, last index fastest) and 16-byte aligned.  The library never
+ *     allocates, frees or retains them.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16_t storage).
+ *   - T is the number of packed tokens; the query and KV token axes coincide
+ *     (packed thd layout), so kv has T rows and every index addresses a row of
+ *     that packed axis directly.
+ *   - A top-k slot is valid iff 0 <= index < T.  -1 is the padding sentinel;
+ *     any other out-of-range value is a caller error (see
+ *     sparse_mla_check_indices) and is treated exactly like -1.
+ *   - Supported shapes: H in {8, 16, 32, 64, 128}; topk > 0 and topk % 64 == 0;
+ *     the head dims are fixed at 576 (q, k) and 512 (v, out).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Compute calls are asynchronous on it and never synchronize
+ *     the host, except sparse_mla_check_indices.
+ *   - Return value: 0 on success, else a negative errno value and a message
+ *     readable with sparse_mla_last_error() on the same host thread:
+ *        -EINVAL  (-22) bad shape, pointer, alignment, scale or workspace size
+ *        -ENOTSUP (-95) the current device is not sm_103, or a mode that is
+ *                       not built
+ *        -EIO     (-5)  a CUDA error was reported while launching
+ *     No work is launched when the call returns -EINVAL or -ENOTSUP.
+ *     Exceptions never cross this boundary.
+ *   - The library needs the CUDA device that owns the pointers to be current.
+ */
+#ifndef SPARSE_MLA_H_
+#define SPARSE_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t smla_bf16_t;  /* bfloat16 bit pattern */
+
+#define SMLA_D_QK 576          /* 512 latent + 64 rope tail */
+#define SMLA_D_V 512           /* latent width = value width */
+#define SMLA_DKV_ATOMIC 0      /* dKV scatter by fp32 vector atomics */
+#define SMLA_DKV_DETERMINISTIC 1  /* reserved: sorted segmented reduction */
+
+/* fp32 LSE written for a row with no valid slot: ln(1e-30) rounded to fp32
+ * (the 1e-30 floor of the miles PR #2079 forward fragment, empty max read
+ * as 0). */
+#define SMLA_LSE_EMPTY (-69.0775527898f)
+
+/*
+ * Forward (miles PR #2079, forward fragment `main`).
+ *   q        [T, H, 576] bf16   queries (absorbed latent 512 + rope 64)
+ *   kv       [T, 1, 576] bf16   latent KV rows; kv[:, :, :512] is also V
+ *   indices  [T, 1, topk] int32 top-k KV rows per query, -1 = padding
+ *   cu_seqlens [B+1] int32 or NULL  sequence boundaries of the packed layout;
+ *            accepted for interface parity, not read by this call
+ *   scale    softmax scale applied to q.k (e.g. 1/sqrt(576)); must be finite
+ *   out      [T, H, 512] bf16   softmax(scale q K^T) V over the valid slots;
+ *            exactly 0 for a row with no valid slot
+ *   lse      [T, H] fp32        natural-log log-sum-exp of the scaled scores;
+ *            SMLA_LSE_EMPTY for a row with no valid slot
+ */
+int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
+                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                   smla_bf16_t* out, float* lse, void* stream);
+
+/* Bytes of device workspace sparse_mla_bwd needs for these sizes (0 if the
+ * sizes are invalid).  The workspace holds Delta = rowsum(dO * out), [T, H]
+ * fp32, and is fully overwritten by each call. */
+size_t sparse_mla_bwd_workspace_bytes(int T, int H, int topk, int dkv_mode);
+
+/*
+ * Backward (slime issue #2201 "Strongest repro evidence";
+ * miles PR #2079, backward fragment `sparse_mla_bwd_kernel`).
+ *   q, kv, indices, cu_seqlens, scale  as for sparse_mla_fwd
+ *   out      [T, H, 512] bf16   forward output (used only for Delta)
+ *   dout     [T, H, 512] bf16   gradient of the loss w.r.t. out
+ *   lse      [T, H] fp32        forward LSE (natural log)
+ *   dkv_mode SMLA_DKV_ATOMIC (SMLA_DKV_DETERMINISTIC returns -ENOTSUP)
+ *   dq       [T, H, 576] bf16   gradient w.r.t. q; exactly 0 on empty rows
+ *   dkv_f32  [T, 1, 576] fp32   gradient w.r.t. kv; zeroed and then
+ *            scatter-added by this call (rows no valid slot names stay 0)
+ *   dkv      [T, 1, 576] bf16 or NULL  round-to-nearest-even copy of dkv_f32
+ *   workspace, workspace_bytes  device scratch of at least
+ *            sparse_mla_bwd_workspace_bytes(T, H, topk, dkv_mode) bytes,
+ *            owned by the caller; it must not be used by another call that
+ *            runs concurrently on the GPU
+ */
+int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                   const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                   int dkv_mode, smla_bf16_t* dq, float* dkv_f32, smla_bf16_t* dkv,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Index validation (Megatron-Bridge PR #17, Bug fixes: top-k padded with
+ * -1).  Counts the entries of indices [T, 1, topk] that are neither -1 nor a
+ * row of their own query's sequence [cu_seqlens[b], cu_seqlens[b+1]).
+ * cu_seqlens [B+1] int32 (device) must start at 0, be non-decreasing and end
+ * at T.  Writes the count to *n_bad (HOST pointer).  This call allocates a
+ * small device counter on `stream` and synchronizes that stream.
+ */
+int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
+                             int B, int64_t* n_bad, void* stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* sparse_mla_last_error(void);
+
+/* Library version string. */
+const char* sparse_mla_version(void);
+
+/* Number of CUDA kernels this process has launched through the library so
+ * far (all threads, all devices).  Diagnostics only: benchmarks read it
+ * before and after a timed region to count the library's launches. */
+uint64_t sparse_mla_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H_ */

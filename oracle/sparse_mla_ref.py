@@ -93,20 +93,27 @@ def fwd_row(q_t: np.ndarray, kv: np.ndarray, J: np.ndarray, scale: float):
     return out, m + np.log(l)
 
 
-def sparse_mla_fwd(q, kv, indices, scale: float, rows=None):
-    """Forward over all tokens (or the listed `rows`).
+def _row(x: np.ndarray, t: int) -> np.ndarray:
+    """Row t of a bf16-bit (uint16) or float array, as float64."""
+    return bf16_bits_to_f64(x[t]) if x.dtype == np.uint16 else np.asarray(x[t], dtype=np.float64)
 
-    q [T, H, 576], kv [T, 1, 576] (or [T, 576]), indices [T, 1, topk] int32.
-    Returns out [T, H, 512] f64 and lse [T, H] f64 (zeros on rows not listed).
+
+def sparse_mla_fwd(q, kv, indices, scale: float, rows=None):
+    """Forward over all tokens, or only over the tokens listed in `rows`.
+
+    q [T, H, 576], kv [T, 1, 576] (or [T, 576]), indices [T, 1, topk] int32;
+    q and kv may be bf16 bit patterns (uint16) or floats.
+    Returns out [n, H, 512] f64 and lse [n, H] f64, where n = T and row i is
+    token i, or n = len(rows) and row i is token rows[i].
     """
-    q = _as_f64(q)
-    kv = _as_f64(kv).reshape(q.shape[0] if kv.ndim == 2 else kv.shape[0], D_QK)
-    T, H, _ = q.shape
+    T, H = q.shape[0], q.shape[1]
+    kvf = _as_f64(kv).reshape(-1, D_QK)
     idx = np.asarray(indices).reshape(T, -1)
-    out = np.zeros((T, H, D_LATENT))
-    lse = np.zeros((T, H))
-    for t in (range(T) if rows is None else rows):
-        out[t], lse[t] = fwd_row(q[t], kv, valid_slots(idx[t], kv.shape[0]), scale)
+    toks = range(T) if rows is None else [int(t) for t in rows]
+    out = np.zeros((len(toks), H, D_LATENT))
+    lse = np.zeros((len(toks), H))
+    for i, t in enumerate(toks):
+        out[i], lse[i] = fwd_row(_row(q, t), kvf, valid_slots(idx[t], kvf.shape[0]), scale)
     return out, lse
 
 
@@ -141,24 +148,26 @@ def bwd_row(q_t, kv, out_t, dout_t, lse_t, J, scale: float):
 
 
 def sparse_mla_bwd(q, kv, out, dout, lse, indices, scale: float, rows=None):
-    """Backward over all tokens (or only `rows`).
+    """Backward over all tokens, or only over the tokens listed in `rows`.
 
-    Returns dq [T, H, 576] f64 and dkv [T, 576] f64.  dkv is the scatter-add of
-    every processed token's per-slot gradient into the row its slot names;
-    rows that no processed slot names stay exactly zero.
+    q [T, H, 576] and dout [T, H, 512] are full (bf16 bits or floats);
+    out and lse hold one entry per processed token: [T, H, 512] / [T, H]
+    when rows is None, else [len(rows), H, 512] / [len(rows), H] aligned
+    with rows.  Returns dq [n, H, 576] f64 (same row convention as out) and
+    dkv [T, 576] f64: the scatter-add of every processed token's per-slot
+    gradient into the row its slot names.  Rows no processed slot names stay
+    exactly zero.
     """
-    q = _as_f64(q)
-    T, H, _ = q.shape
-    kv = _as_f64(kv).reshape(-1, D_QK)
-    out = _as_f64(out).reshape(T, H, D_LATENT)
-    dout = _as_f64(dout).reshape(T, H, D_LATENT)
-    lse = np.asarray(lse, dtype=np.float64).reshape(T, H)
+    T, H = q.shape[0], q.shape[1]
+    kvf = _as_f64(kv).reshape(-1, D_QK)
     idx = np.asarray(indices).reshape(T, -1)
-    dq = np.zeros((T, H, D_QK))
-    dkv = np.zeros((kv.shape[0], D_QK))
-    for t in (range(T) if rows is None else rows):
-        J = valid_slots(idx[t], kv.shape[0])
-        dq[t], J, G = bwd_row(q[t], kv, out[t], dout[t], lse[t], J, scale)
+    toks = range(T) if rows is None else [int(t) for t in rows]
+    dq = np.zeros((len(toks), H, D_QK))
+    dkv = np.zeros((kvf.shape[0], D_QK))
+    for i, t in enumerate(toks):
+        J = valid_slots(idx[t], kvf.shape[0])
+        dq[i], J, G = bwd_row(_row(q, t), kvf, _row(out, i), _row(dout, t),
+                              np.asarray(lse[i], dtype=np.float64), J, scale)
         if J.size:
             np.add.at(dkv, J, G)
     return dq, dkv

@@ -142,10 +142,10 @@ def pin_closed_forms(orc, seed: int = 3) -> float:
     # one valid slot: token 5 -> row 9, slot position 6
     idx[5, 6] = 9
     out, lse = orc.sparse_mla_fwd(q, kv, idx, scale)
-    dq, dkv = orc.sparse_mla_bwd(q, kv, out, dout, lse, idx, scale, rows=[5])
+    dq, dkv = orc.sparse_mla_bwd(q, kv, out[[5]], dout, lse[[5]], idx, scale, rows=[5])
     err = max(err, np.abs(out[5] - kv[9, :D][None]).max())
     err = max(err, np.abs(lse[5] - scale * (q[5] @ kv[9])).max())
-    err = max(err, np.abs(dq[5]).max())
+    err = max(err, np.abs(dq[0]).max())
     err = max(err, np.abs(dkv[9, :D] - dout[5].sum(0)).max())
     err = max(err, np.abs(dkv[9, D:]).max())
     # identical rows: rows 1, 4, 11 share content; token 7 lists them; token 8 lists row 2 three times

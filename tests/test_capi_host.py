@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point the header declares, and rejects bad
+arguments before touching the device (every call here returns before any
+CUDA call is made, so fake aligned pointers are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_sparse_mla_gb300 import build as B
+from bwd_sparse_mla_gb300 import capi
+
+HEADER = os.path.join(B.ROOT, "include", "sparse_mla.h")
+EINVAL, ENOTSUP = -22, -95
+FAKE = ctypes.c_void_p(0x10000)        # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    srcs = B.sources() + [HEADER]
+    stale = (not os.path.exists(B.LIB) or
+             max(os.path.getmtime(s) for s in srcs + [os.path.join(B.CSRC, "smla_common.cuh")])
+             > os.path.getmtime(B.LIB))
+    if stale:
+        B.build()
+    return capi.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(sparse_mla_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert {"sparse_mla_fwd", "sparse_mla_bwd", "sparse_mla_bwd_workspace_bytes",
+            "sparse_mla_check_indices", "sparse_mla_last_error", "sparse_mla_version"} <= set(syms)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_version(lib):
+    assert "sm_103a" in capi.sparse_mla_version()
+
+
+def _fwd(lib, T=16, H=8, topk=64, scale=0.04, q=FAKE, kv=FAKE, idx=FAKE, out=FAKE, lse=FAKE):
+    return lib.sparse_mla_fwd(q, kv, idx, None, T, H, topk, 1, scale, out, lse, None)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(H=7), "H must be"),
+    (dict(H=256), "H must be"),
+    (dict(topk=100), "topk"),
+    (dict(topk=0), "topk"),
+    (dict(T=-1), "T must be"),
+    (dict(scale=float("nan")), "scale"),
+    (dict(scale=float("inf")), "scale"),
+    (dict(q=None), "q must not be NULL"),
+    (dict(lse=None), "lse must not be NULL"),
+    (dict(kv=MISALIGNED), "kv must be 16-byte aligned"),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, msg):
+    assert _fwd(lib, **kw) == EINVAL
+    assert msg in capi.sparse_mla_last_error()
+
+
+def test_fwd_empty_is_a_noop(lib):
+    assert _fwd(lib, T=0, q=None, kv=None, idx=None, out=None, lse=None) == 0
+    assert capi.sparse_mla_last_error() == ""
+
+
+def _bwd(lib, T=16, H=8, topk=64, mode=0, ws=FAKE, ws_bytes=1 << 20, dq=FAKE):
+    return lib.sparse_mla_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, T, H, topk, 1, 0.04, mode,
+                              dq, FAKE, None, ws, ws_bytes, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert _bwd(lib, mode=1) == ENOTSUP
+    assert "DETERMINISTIC" in capi.sparse_mla_last_error()
+    assert _bwd(lib, mode=7) == EINVAL
+    assert _bwd(lib, ws_bytes=16) == EINVAL
+    assert "workspace too small" in capi.sparse_mla_last_error()
+    assert _bwd(lib, ws=None) == EINVAL
+    assert _bwd(lib, dq=MISALIGNED) == EINVAL
+    assert _bwd(lib, H=12) == EINVAL
+    assert _bwd(lib, T=0) == 0
+
+
+def test_workspace_bytes(lib):
+    assert capi.sparse_mla_bwd_workspace_bytes(1000, 128, 2048) >= 1000 * 128 * 4
+    assert capi.sparse_mla_bwd_workspace_bytes(1000, 12, 2048) == 0
+    assert capi.sparse_mla_bwd_workspace_bytes(1000, 8, 100) == 0
+    assert capi.sparse_mla_bwd_workspace_bytes(1000, 8, 64, 1) == 0
+
+
+def test_check_indices_rejects_bad_arguments(lib):
+    n = ctypes.c_int64(-1)
+    assert lib.sparse_mla_check_indices(FAKE, 16, 64, FAKE, 0, ctypes.byref(n), None) == EINVAL
+    assert lib.sparse_mla_check_indices(FAKE, 16, 64, None, 1, ctypes.byref(n), None) == EINVAL
+    assert lib.sparse_mla_check_indices(FAKE, 16, 64, FAKE, 1, None, None) == EINVAL
+    assert lib.sparse_mla_check_indices(None, 0, 64, None, 1, ctypes.byref(n), None) == 0
+    assert n.value == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(capi, "_lib", None)
+    monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        capi.load()

@@ -112,8 +112,8 @@ MUTANTS = {
                          "dq_t = dS @ K"),
     "delta from the wrong operand": ("dlt = (dout_t * out_t).sum(axis=1)          # Delta from the given output",
                                      "dlt = (dout_t * dout_t).sum(axis=1)"),
-    "lse in base 2": ("return out, m + np.log(l)\n\n\ndef sparse_mla_fwd",
-                      "return out, (m + np.log(l)) / np.log(2.0)\n\n\ndef sparse_mla_fwd"),
+    "lse in base 2": ("return out, m + np.log(l)\n\n\ndef _row",
+                      "return out, (m + np.log(l)) / np.log(2.0)\n\n\ndef _row"),
     "padding read as row 0": ("keep = (idx_row >= 0) & (idx_row < T)\n    return idx_row[keep]",
                               "return np.maximum(idx_row, 0)[idx_row < T]"),
     "no sumexp floor on empty rows": ("m = np.zeros(H)\n        l = np.maximum(np.zeros(H), SUMEXP_FLOOR)",
