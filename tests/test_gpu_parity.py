@@ -73,13 +73,18 @@ def test_bwd_small(small):
 
 
 def test_fwd_bwd_chain_small(small):
-    """GPU forward feeding GPU backward vs the oracle chain in fp64."""
+    """GPU forward feeding GPU backward vs the oracle chain.  The backward's
+    `out` argument is bf16 in this interface, so the oracle chain hands its
+    backward the oracle output rounded to bf16 as well: with a near one-hot
+    softmax, dS = P (dP - Delta) cancels and Delta inherits the bf16 rounding
+    of `out`, which no kernel can undo."""
     w, d, (q, kv, dout), (out_ref, lse_ref) = small
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
     dq, dkv32, _ = capi.sparse_mla_bwd(d["q"], d["kv"], out, d["dout"], lse, d["indices"],
                                        d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
-    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, out_ref, dout, lse_ref, w.indices, w.scale)
+    out_bf16 = torch.tensor(out_ref, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, out_bf16, dout, lse_ref, w.indices, w.scale)
     assert_close("dq(chain)", to_f64(dq), dq_ref)
     assert_close("dkv(chain)", to_f64(dkv32).reshape(w.T, -1), dkv_ref)
 
