@@ -49,6 +49,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_last_error.restype = ctypes.c_char_p
     lib.sparse_mla_version.argtypes = []
     lib.sparse_mla_version.restype = ctypes.c_char_p
+    lib.sparse_mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
+    lib.sparse_mla_device_status.restype = I
     lib.sparse_mla_launch_count.argtypes = []
     lib.sparse_mla_launch_count.restype = ctypes.c_uint64
     _lib = lib
@@ -65,6 +67,12 @@ def sparse_mla_version() -> str:
 
 def sparse_mla_launch_count() -> int:
     return int(load().sparse_mla_launch_count())
+
+
+def sparse_mla_device_status(clear: bool = False) -> int:
+    st = ctypes.c_uint32(0)
+    _check(load().sparse_mla_device_status(ctypes.byref(st), int(clear)))
+    return int(st.value)
 
 
 def _check(rc: int) -> None:

@@ -80,6 +80,16 @@ const char* sparse_mla_version(void) { return "sparse_mla_gb300 0.1.0 (sm_103a)"
 
 uint64_t sparse_mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int sparse_mla_device_status(uint32_t* status, int clear) {
+  g_last_error.clear();
+  if (status == nullptr) return fail(-EINVAL, "status must not be NULL");
+  if (int r = check_device()) return r;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = smla::read_tc_status(status, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_device_status");
+  return 0;
+}
+
 int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
                    const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
                    smla_bf16_t* out, float* lse, void* stream) {
@@ -95,7 +105,8 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
   SMLA_REQUIRE_PTR(lse);
   if (int r = check_device()) return r;
   smla::FwdArgs a{q, kv, indices, out, lse, T, H, topk, scale};
-  cudaError_t e = smla::launch_fwd_simt(a, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (H == 128) ? smla::launch_fwd_tc(a, s) : smla::launch_fwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_fwd launch");
   count_launches(1);
   return 0;

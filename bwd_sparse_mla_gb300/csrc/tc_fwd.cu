@@ -1,0 +1,370 @@
+// Tensor-core (tcgen05) forward for H = 128 heads.
+//
+// Work split: a cluster of two CTAs handles one query token.  The 576-wide
+// key dimension is split between them (CTA 0: dims [0,256), CTA 1: dims
+// [256,576)), and so is the 512-wide value/output dimension (CTA 0: [0,256),
+// CTA 1: [256,512)).  Each CTA gathers only its own columns of the named KV
+// rows, so the pair reads every gathered byte exactly once, and each CTA
+// holds an O accumulator of 128 heads x 256 dims (256 TMEM columns).  The
+// partial scores of the two halves are exchanged through distributed shared
+// memory and summed in both CTAs (a + b == b + a, so both see bit-identical
+// scores and take identical softmax decisions).
+//
+// Per block of 64 top-k slots:
+//   producer warp : reads the 64 indices, masks them (valid iff 0 <= idx < T),
+//                   and gathers the rows with TMA gather4 into 128B-swizzled
+//                   shared memory; padding slots use an out-of-range row, so
+//                   TMA fills them with zeros (exact-zero K and V, as in the
+//                   miles PR #2079 fix, implementation breakdown item 2);
+//   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
+//                   into TMEM, then O += P V_half (M=128, N=256, K=64);
+//   softmax warps : one thread per head: load the 64 partial scores, swap
+//                   halves with the peer CTA, mask padding to -inf, online
+//                   softmax in the exp2 domain with a lazily updated running
+//                   max, rescale O in TMEM when the max moves, write P (bf16)
+//                   for the PV MMA.  At the end the sum of exponentials is
+//                   floored at 1e-30 (PR #2079 forward fragment), so a row
+//                   with no valid slot gets out = 0 and LSE = ln(1e-30).
+#include <cuda.h>
+
+#include "smla_common.cuh"
+#include "tc_common.cuh"
+
+namespace smla {
+namespace {
+
+using namespace tc;
+
+constexpr int kBK = 64;                 // slots per block
+constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA, warps 2..5 softmax
+constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
+constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
+constexpr int kStageBytes = 5 * kChunkKV;
+constexpr int kXPitch = 272;            // bytes per exchanged score row (64 fp32 + pad)
+constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int SM_Q = 0;
+constexpr int SM_KV = SM_Q + 5 * kChunkQ;           // 2 stages
+constexpr int SM_P = SM_KV + 2 * kStageBytes;
+constexpr int SM_X = SM_P + 128 * 128;
+constexpr int SM_MASK = SM_X + 128 * kXPitch;       // 2 x u64
+constexpr int SM_BAR = SM_MASK + 16;
+enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 10,
+           P_FULL = 11, O_DONE = 12, NBAR = 13 };
+constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
+constexpr int SM_ABORT = SM_TMEM + 4;
+constexpr int kSmemBytes = SM_ABORT + 4 + 1024;     // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_O = 0;            // 256 columns
+constexpr uint32_t TM_S = 256;          // 2 x 64 columns
+
+struct TcFwdParams {
+  const int32_t* indices;
+  uint16_t* out;
+  float* lse;
+  uint32_t* status;
+  int T, topk;
+  float c2;                             // scale * log2(e)
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
+
+__global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
+    tc_fwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                       TcFwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned (128B swizzle atoms)
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();          // 0 or 1
+  const uint32_t peer = crank ^ 1u;
+  const int t = blockIdx.x >> 1;
+  const int nch = 4 + (int)crank;                     // 64-dim key chunks of this CTA
+  const int g0 = 4 * (int)crank;                      // first global chunk
+  const int nblk = p.topk / kBK;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_addr(sb, KV_FULL + 0), 1);
+    mbar_init(bar_addr(sb, KV_FULL + 1), 1);
+    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1);
+    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1);
+    mbar_init(bar_addr(sb, Q_FULL), 1);
+    mbar_init(bar_addr(sb, S_FULL + 0), 1);
+    mbar_init(bar_addr(sb, S_FULL + 1), 1);
+    mbar_init(bar_addr(sb, S_FREE + 0), 128);
+    mbar_init(bar_addr(sb, S_FREE + 1), 128);
+    mbar_init(bar_addr(sb, X_FULL), 128);       // arrivals from the peer's 128 softmax threads
+    mbar_init(bar_addr(sb, X_EMPTY), 128);
+    mbar_init(bar_addr(sb, P_FULL), 128);
+    mbar_init(bar_addr(sb, O_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SM_TMEM, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer's barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kv);
+      mbar_arrive_expect_tx(bar_addr(sb, Q_FULL), nch * kChunkQ);
+      for (int k = 0; k < nch; ++k)
+        tma_load_2d(sb + SM_Q + k * kChunkQ, &tm_q, 64 * (g0 + k), t * 128, bar_addr(sb, Q_FULL));
+    }
+    const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      int ok = 1;
+      if (i >= 2 && lane == 0) ok = mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // warp-uniform exit
+      const int a = __ldg(irow + i * kBK + lane);
+      const int b = __ldg(irow + i * kBK + 32 + lane);
+      const bool va = (a >= 0 && a < p.T), vb = (b >= 0 && b < p.T);
+      const int ra = va ? a : p.T;      // row T is out of range: TMA fills zeros
+      const int rb = vb ? b : p.T;
+      const uint32_t ma = __ballot_sync(0xffffffffu, va), mbk = __ballot_sync(0xffffffffu, vb);
+      if (lane == 0) {
+        *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st) = (uint64_t)ma | ((uint64_t)mbk << 32);
+        mbar_arrive_expect_tx(bar_addr(sb, KV_FULL + st), nch * kChunkKV);
+      }
+      __syncwarp();
+      // lane g < 16 gathers slots 4g .. 4g+3
+      int rows[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int slot = 4 * (lane & 15) + k;
+        const int xa = __shfl_sync(0xffffffffu, ra, slot & 31);
+        const int xb = __shfl_sync(0xffffffffu, rb, slot & 31);
+        rows[k] = slot < 32 ? xa : xb;
+      }
+      if (lane < 16) {
+        const uint32_t dst = sb + SM_KV + st * kStageBytes + lane * 4 * 128;
+        for (int k = 0; k < nch; ++k)
+          tma_gather4(dst + k * kChunkKV, &tm_kv, 64 * (g0 + k), rows[0], rows[1], rows[2], rows[3],
+                      bar_addr(sb, KV_FULL + st));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
+      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      bool ok = mbar_wait(bar_addr(sb, Q_FULL), 0, abort_flag, p.status);
+      for (int i = 0; ok && i <= nblk; ++i) {
+        if (i < nblk) {
+          const int st = i & 1, b = i & 1;
+          if (!mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)) break;
+          if (i >= 2 && !mbar_wait(bar_addr(sb, S_FREE + b), ((i - 2) >> 1) & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          for (int k = 0; k < nch; ++k) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = sdesc_sw128(sb + SM_Q + k * kChunkQ + ks * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sb + SM_KV + st * kStageBytes + k * kChunkKV + ks * 32, 16, 1024);
+              mma_bf16_ss(tmem + TM_S + 64 * b, ad, bd, idesc_s, (k | ks) != 0);
+            }
+          }
+          mma_commit(bar_addr(sb, S_FULL + b));
+        }
+        if (i >= 1) {
+          const int j = i - 1, stj = j & 1;
+          if (!mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = sdesc_sw128(sb + SM_P + ks * 32, 16, 1024);
+            // V is the first four chunks of the stage, read MN-major:
+            // LBO = stride between 64-dim chunks, SBO = stride between 8-row groups
+            const uint64_t bd = sdesc_sw128(sb + SM_KV + stj * kStageBytes + ks * 16 * 128, kChunkKV, 1024);
+            mma_bf16_ss(tmem + TM_O, ad, bd, idesc_pv, (j > 0 || ks > 0));
+          }
+          mma_commit(bar_addr(sb, O_DONE));
+          mma_commit(bar_addr(sb, KV_EMPTY + stj));
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+    const int h = 32 * q4 + lane;            // head == TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xrow = sb + SM_X + h * kXPitch;
+    const uint32_t xrow_peer = mapa(xrow, peer);
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    uint8_t* prow = smem + SM_P + h * 128;
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      const int b = i & 1, st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (i >> 1) & 1, abort_flag, p.status)))) break;
+      tc_fence_after();
+      float s[64];
+      tmem_ld64(tl + TM_S + 64 * b, s);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, S_FREE + b));
+      // swap partial scores with the peer CTA
+      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
+#pragma unroll
+      for (int v = 0; v < 16; ++v) st_cluster_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+      mbar_arrive_remote(xfull_peer);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
+      const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        const float4 o = xr[v];
+        s[4 * v] += o.x; s[4 * v + 1] += o.y; s[4 * v + 2] += o.z; s[4 * v + 3] += o.w;
+      }
+      mbar_arrive_remote(xempty_peer);
+      // slot validity of this block (written by the producer before it armed KV_FULL)
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
+      const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        s[j] = ((mask >> j) & 1ull) ? s[j] * p.c2 : -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      // lazily updated running max: move it only when the block max exceeds it by > 8 (log2 units)
+      const bool move = mx > m_run + kLazyRescale;
+      const float m_new = move ? mx : m_run;
+      const float alpha = move ? ex2(m_run - m_new) : 1.f;   // m_run = -inf gives 0
+      float sum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = ex2(s[2 * j] - m_new), p1 = ex2(s[2 * j + 1] - m_new);   // -inf -> 0
+        sum += p0 + p1;
+        pk[j] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      m_run = m_new;
+      // P buffer and O are free once the previous PV has completed
+      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (i - 1) & 1, abort_flag, p.status)))) break;
+      tc_fence_after();
+      if (i >= 1 && __any_sync(0xffffffffu, move)) {
+#pragma unroll 1
+        for (int part = 0; part < 4; ++part) {
+          float o[64];
+          tmem_ld64(tl + TM_O + 64 * part, o);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) o[j] *= alpha;
+          tmem_st64(tl + TM_O + 64 * part, o);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, P_FULL));
+    }
+    if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (nblk - 1) & 1, abort_flag, p.status));
+    tc_fence_after();
+    if (ok) {
+      const float inv = 1.f / fmaxf(l, kSumexpFloor);
+      uint16_t* orow = p.out + ((int64_t)t * 128 + h) * kDv + 256 * crank;
+#pragma unroll 1
+      for (int part = 0; part < 4; ++part) {
+        float o[64];
+        tmem_ld64(tl + TM_O + 64 * part, o);
+        uint4* dst = reinterpret_cast<uint4*>(orow + 64 * part);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                              pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+      }
+      if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (*abort_flag) __nanosleep(1000000);   // let copies and MMAs already issued land
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer no longer touches this CTA's shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+__device__ uint32_t g_status = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, 576] with a box of `box_rows` x 64 columns, 128B swizzle.
+bool make_map_576(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {576, rows};
+  cuuint64_t strides[1] = {576 * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+uint32_t* tc_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+  return static_cast<uint32_t*>(p);
+}
+
+cudaError_t read_tc_status(uint32_t* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_status, &z, sizeof(z));
+  }
+  return e;
+}
+
+cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
+  CUtensorMap tm_q, tm_kv;
+  if (!make_map_576(&tm_q, a.q, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
+  if (!make_map_576(&tm_kv, a.kv, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
+  uint32_t* status = tc_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  TcFwdParams p{a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
+  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

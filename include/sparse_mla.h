@@ -131,6 +131,13 @@ const char* sparse_mla_last_error(void);
 /* Library version string. */
 const char* sparse_mla_version(void);
 
+/* Reads the status word of the tensor-core kernels on the current device
+ * into *status (HOST pointer): 0 = every bounded wait inside those kernels
+ * completed; 1 = some wait gave up after its time limit, the kernel returned
+ * early and the outputs of that call are not valid.  With clear != 0 the
+ * word is reset to 0.  Synchronizes with the device. */
+int sparse_mla_device_status(uint32_t* status, int clear);
+
 /* Number of CUDA kernels this process has launched through the library so
  * far (all threads, all devices).  Diagnostics only: benchmarks read it
  * before and after a timed region to count the library's launches. */

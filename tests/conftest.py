@@ -19,3 +19,16 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(request):
+    """After every GPU test: no bounded wait inside a tensor-core kernel gave up."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    from bwd_sparse_mla_gb300 import capi
+    assert capi.sparse_mla_device_status(clear=True) == 0, "a kernel wait timed out"
