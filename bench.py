@@ -202,7 +202,12 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     capi.load()
 
-    w = W.make_workload(args.config)
+    if args.tokens:
+        w = W.make_workload(args.config, values=False)
+        W.draw_values(w, rows=range(args.tokens))
+        w = W.truncate(w, args.tokens)
+    else:
+        w = W.make_workload(args.config)
     n_valid = w.n_valid()
     T, H, topk = w.T, w.H, w.topk
 
@@ -414,6 +419,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, help="workload 1..5 (5 = headline)")
+    ap.add_argument("--tokens", type=int, default=0, help="use only the first N tokens (small profiling case)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=8)

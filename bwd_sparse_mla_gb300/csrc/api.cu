@@ -153,7 +153,7 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
-  e = smla::launch_bwd_simt(a, s);
+  e = (H == 128) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
   count_launches(1);
   if (dkv != nullptr) {

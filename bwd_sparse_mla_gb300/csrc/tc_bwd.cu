@@ -1,0 +1,407 @@
+// Tensor-core (tcgen05) backward for H = 128 heads.
+//
+// Work split: as in the forward, a cluster of two CTAs handles one query
+// token and splits the feature dimension: CTA 0 owns key dims [0,256) and
+// value dims [0,256); CTA 1 owns key dims [256,576) (the rope tail included)
+// and value dims [256,512).  Each CTA keeps its slice of q and dO for the
+// token in shared memory, accumulates its slice of dQ (128 heads x 256|320
+// dims) in TMEM, and produces its slice of every dKV row.
+//
+// Per block of 32 top-k slots:
+//   producer : masked TMA gather4 of the CTA's columns of the 32 named rows
+//              (padding slots read an out-of-range row: exact zeros);
+//   MMA      : S_half = q_half K_half^T and dP_half = dO_half V_half^T
+//              (M=128 heads, N=32 slots) into TMEM;
+//   softmax  : one thread per head swaps its partial S and dP rows with the
+//              peer CTA through distributed shared memory, sums them
+//              (both CTAs obtain bit-identical sums), recomputes
+//              P = exp2(S*scale*log2e - lse*log2e) (0 on padding slots),
+//              dS' = scale * P * (dP - Delta), and stores P and dS' as bf16;
+//   MMA      : dQ_half += dS' K_half (M=128, N=256|320, K=32) and the
+//              transposed dKV tiles dKV^T[d, j] = dO^T P + q^T dS'
+//              (M=128 dims, N=32 slots, K=128 heads);
+//   drain    : four warps read the dKV tiles from TMEM and add them into the
+//              fp32 dKV rows named by the valid slots (coalesced 128-byte
+//              fp32 reductions; padding slots issue no write, the no-op the
+//              miles PR #2079 summary describes for the clamped atomic).
+#include <cuda.h>
+
+#include "smla_common.cuh"
+#include "tc_common.cuh"
+
+namespace smla {
+namespace {
+
+using namespace tc;
+
+constexpr int kBK = 32;
+constexpr int kThreads = 320;           // w0 producer, w1 MMA, w2..5 softmax, w6..9 dKV drain
+constexpr int kChunk = 128 * 128;       // 64-dim chunk of q / dO for 128 heads
+constexpr int kChunkKV = kBK * 128;     // 64-dim chunk of a 32-row KV block
+constexpr int kStage = 5 * kChunkKV;
+constexpr int kXPitch = 272;
+
+constexpr int SM_Q = 0;                                 // 5 chunks
+constexpr int SM_DO = SM_Q + 5 * kChunk;                // 4 chunks
+constexpr int SM_KV = SM_DO + 4 * kChunk;               // 2 stages
+constexpr int SM_X = SM_KV + 2 * kStage;                // exchange rows, then P / dS
+constexpr int SM_P = SM_X;                              // 128 rows x 64 B, 64B swizzle
+constexpr int SM_DS = SM_X + 128 * 64;
+constexpr int SM_ROWS = SM_X + 128 * kXPitch;           // 2 x 32 int32
+constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
+constexpr int SM_BAR = SM_MASK + 8;
+enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 8,
+           P_FULL = 9, PDS_FREE = 10, DKV_FULL = 11, DKV_FREE = 12, NBAR = 13 };
+constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
+constexpr int SM_ABORT = SM_TMEM + 4;
+constexpr int kSmemBytes = SM_ABORT + 4 + 1024;
+static_assert(SM_X % 1024 == 0, "swizzle atoms");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_DQ = 0;           // up to 320 columns
+constexpr uint32_t TM_S = 320;          // 32
+constexpr uint32_t TM_DP = 352;         // 32
+constexpr uint32_t TM_DKV = 384;        // up to 3 tiles x 32
+
+struct TcBwdParams {
+  const int32_t* indices;
+  const float* lse;
+  const float* delta;
+  uint16_t* dq;
+  float* dkv32;
+  uint32_t* status;
+  int T, topk;
+  float scale, c2;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
+
+__global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
+    tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_do, TcBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t peer = crank ^ 1u;
+  const int t = blockIdx.x >> 1;
+  const int nch = 4 + (int)crank;          // key chunks (64 dims each) of this CTA
+  const int g0 = 4 * (int)crank;           // first global key chunk; value chunks are g0 .. g0+3
+  const int ntile = 2 + (int)crank;        // 128-dim dKV tiles
+  const int ndq = 64 * nch;                // dQ columns
+  const int nblk = p.topk / kBK;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_addr(sb, KV_FULL + 0), 1);
+    mbar_init(bar_addr(sb, KV_FULL + 1), 1);
+    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 128);   // MMA commit + drain threads (row list read)
+    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 128);
+    mbar_init(bar_addr(sb, QD_FULL), 1);
+    mbar_init(bar_addr(sb, SDP_FULL), 1);
+    mbar_init(bar_addr(sb, SDP_FREE), 128);
+    mbar_init(bar_addr(sb, X_FULL), 128);
+    mbar_init(bar_addr(sb, X_EMPTY), 128);
+    mbar_init(bar_addr(sb, P_FULL), 128);
+    mbar_init(bar_addr(sb, PDS_FREE), 1);
+    mbar_init(bar_addr(sb, DKV_FULL), 1);
+    mbar_init(bar_addr(sb, DKV_FREE), 128);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SM_TMEM, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kv);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (nch + 4) * kChunk);
+      for (int k = 0; k < nch; ++k)
+        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
+      for (int k = 0; k < 4; ++k)
+        tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
+    }
+    const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    int* srows = reinterpret_cast<int*>(smem + SM_ROWS);
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      int ok = 1;
+      if (i >= 2 && lane == 0) ok = mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int a = __ldg(irow + i * kBK + lane);
+      const bool va = (a >= 0 && a < p.T);
+      const int ra = va ? a : p.T;         // out-of-range row: TMA fills zeros
+      const uint32_t m = __ballot_sync(0xffffffffu, va);
+      srows[st * 32 + lane] = va ? a : -1;
+      __syncwarp();
+      if (lane == 0) {
+        *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st) = m;
+        mbar_arrive_expect_tx(bar_addr(sb, KV_FULL + st), nch * kChunkKV);
+      }
+      __syncwarp();
+      int rows[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rows[k] = __shfl_sync(0xffffffffu, ra, (4 * (lane & 7) + k) & 31);
+      if (lane < 8) {
+        const uint32_t dst = sb + SM_KV + st * kStage + lane * 4 * 128;
+        for (int k = 0; k < nch; ++k)
+          tma_gather4(dst + k * kChunkKV, &tm_kv, 64 * (g0 + k), rows[0], rows[1], rows[2], rows[3],
+                      bar_addr(sb, KV_FULL + st));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_sdp = idesc_bf16(128, kBK, false, false);
+      const uint32_t id_dq256 = idesc_bf16(128, 256, false, true);
+      const uint32_t id_dq64 = idesc_bf16(128, 64, false, true);
+      const uint32_t id_dkv = idesc_bf16(128, kBK, true, true);
+      bool ok = mbar_wait(bar_addr(sb, QD_FULL), 0, abort_flag, p.status);
+      // iteration i issues S/dP of block i, then dQ/dKV of block i-1, so the
+      // score MMAs of the next block run while the softmax warps work
+      for (int i = 0; ok && i <= nblk; ++i) {
+        if (i < nblk) {
+          const int st = i & 1;
+          const uint32_t kvb = sb + SM_KV + st * kStage;
+          if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
+          if (i >= 1 && !(ok = mbar_wait(bar_addr(sb, SDP_FREE), (i - 1) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          // S_half = q_half K_half^T ; dP_half = dO_half V_half^T   (K-major operands, 128B swizzle)
+          for (int k = 0; k < nch; ++k)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_ss(tmem + TM_S, sdesc_sw128(sb + SM_Q + k * kChunk + ks * 32, 16, 1024),
+                          sdesc_sw128(kvb + k * kChunkKV + ks * 32, 16, 1024), id_sdp, (k | ks) != 0);
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_ss(tmem + TM_DP, sdesc_sw128(sb + SM_DO + k * kChunk + ks * 32, 16, 1024),
+                          sdesc_sw128(kvb + k * kChunkKV + ks * 32, 16, 1024), id_sdp, (k | ks) != 0);
+          mma_commit(bar_addr(sb, SDP_FULL));
+        }
+        if (i >= 1) {
+          const int j = i - 1, stj = j & 1;
+          const uint32_t kvb = sb + SM_KV + stj * kStage;
+          if (!(ok = mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          // dQ_half += dS' K_half: A = dS' (K-major, 64B swizzle), B = K block read MN-major
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t ad = sdesc_sw64(sb + SM_DS + ks * 32, 16, 512);
+            mma_bf16_ss(tmem + TM_DQ, ad, sdesc_sw128(kvb + ks * 16 * 128, kChunkKV, 1024), id_dq256,
+                        (j > 0 || ks > 0));
+            if (nch == 5)
+              mma_bf16_ss(tmem + TM_DQ + 256, ad, sdesc_sw128(kvb + 4 * kChunkKV + ks * 16 * 128, kChunkKV, 1024),
+                          id_dq64, (j > 0 || ks > 0));
+          }
+          // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
+          //   dKV^T = q_half^T dS' + dO_half^T P   (A MN-major 128B swizzle, B MN-major 64B swizzle)
+          if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE), (j - 1) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          for (int m = 0; m < ntile; ++m) {
+            const uint32_t d_t = tmem + TM_DKV + 32 * m;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma_bf16_ss(d_t, sdesc_sw128(sb + SM_Q + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024),
+                          sdesc_sw64(sb + SM_DS + ks * 16 * 64, 8192, 512), id_dkv, ks != 0);
+            if (2 * m < 4) {   // tiles inside the value range also get the dO^T P term
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(d_t, sdesc_sw128(sb + SM_DO + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024),
+                            sdesc_sw64(sb + SM_P + ks * 16 * 64, 8192, 512), id_dkv, 1);
+            }
+          }
+          mma_commit(bar_addr(sb, DKV_FULL));
+          mma_commit(bar_addr(sb, PDS_FREE));
+          mma_commit(bar_addr(sb, KV_EMPTY + stj));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax / dS
+    const int q4 = warp & 3;
+    const int h = 32 * q4 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xrow = sb + SM_X + h * kXPitch;
+    const uint32_t xrow_peer = mapa(xrow, peer);
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    const float lse2 = p.lse[(int64_t)t * 128 + h] * kLog2e;
+    const float dl = p.delta[(int64_t)t * 128 + h];
+    uint8_t* prow = smem + SM_P + h * 64;
+    uint8_t* dsrow = smem + SM_DS + h * 64;
+    const int sw = (h >> 1) & 3;        // 64B swizzle: 16-byte chunk index ^= address bits [7,9)
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
+      tc_fence_after();
+      float s[32], dp[32];
+      tmem_ld32(tl + TM_S, s);
+      tmem_ld32(tl + TM_DP, dp);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, SDP_FREE));
+      if (i >= 1) {
+        // this CTA's MMAs are done with its P / dS (which live in its exchange rows):
+        // let the peer write the next partial rows here
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status)))) break;
+        mbar_arrive_remote(xempty_peer);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) st_cluster_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        st_cluster_v4(xrow_peer + 128 + 16 * v, dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
+      mbar_arrive_remote(xfull_peer);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
+      const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = xr[v], b = xr[8 + v];
+        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+        dp[4 * v] += b.x; dp[4 * v + 1] += b.y; dp[4 * v + 2] += b.z; dp[4 * v + 3] += b.w;
+      }
+      named_bar(1, 128);   // every exchange row is read before P / dS overwrite the area
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
+      const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
+      uint32_t pp[16], dd[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
+        const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
+        const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
+        pp[j] = pack_bf16x2(p0, p1);
+        dd[j] = pack_bf16x2(p.scale * p0 * (dp[2 * j] - dl), p.scale * p1 * (dp[2 * j + 1] - dl));
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
+        *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, P_FULL));
+    }
+    if (ok && nblk > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nblk - 1) & 1, abort_flag, p.status));
+    tc_fence_after();
+    if (ok) {
+      uint16_t* qrow = p.dq + ((int64_t)t * 128 + h) * kDqk + 256 * crank;
+#pragma unroll 1
+      for (int part = 0; part < ndq / 64; ++part) {
+        float o[64];
+        tmem_ld64(tl + TM_DQ + 64 * part, o);
+        uint4* dst = reinterpret_cast<uint4*>(qrow + 64 * part);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
+                              pack_bf16x2(o[8 * c + 4], o[8 * c + 5]), pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dKV drain
+    const int q4 = warp & 3;
+    const int L = 32 * q4 + lane;               // TMEM lane = dim within a 128-dim tile
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
+    const int dbase = 256 * (int)crank;          // first key dim of this CTA
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), i & 1, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
+      int rows[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rows[j] = srows[st * 32 + j];
+      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
+      tc_fence_after();
+      float g[3][32];
+#pragma unroll
+      for (int m = 0; m < 3; ++m)
+        if (m < ntile) tmem_ld32(tl + TM_DKV + 32 * m, g[m]);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, DKV_FREE));
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        const int d = dbase + 128 * m + L;
+        if (m < ntile && d < kDqk) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (rows[j] >= 0) red_add_f32(p.dkv32 + (int64_t)rows[j] * kDqk + d, g[m][j]);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (*abort_flag) __nanosleep(1000000);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+uint32_t* tc_status_ptr();
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
+  CUtensorMap tm_q, tm_kv, tm_do;
+  if (!make_map(&tm_q, a.q, kDqk, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tm_kv, a.kv, kDqk, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
+  if (!make_map(&tm_do, a.dout, kDv, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
+  uint32_t* status = tc_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  TcBwdParams p{a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
+  tc_bwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_kv, tm_do, p);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

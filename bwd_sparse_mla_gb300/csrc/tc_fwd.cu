@@ -206,7 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
     uint8_t* prow = smem + SM_P + h * 128;
-    float m_run = -INFINITY, l = 0.f;
+    // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
+    // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
+    float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int b = i & 1, st = i & 1;
@@ -242,15 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const bool move = mx > m_run + kLazyRescale;
       const float m_new = move ? mx : m_run;
       const float alpha = move ? ex2(m_run - m_new) : 1.f;   // m_run = -inf gives 0
-      float sum = 0.f;
+      // while no valid slot has been seen m_new is -inf; subtract 0 instead so
+      // that padding gives exp2(-inf) = 0 and never exp2(-inf - -inf) = NaN
+      const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+      float sum = 0.f, sum_bf = 0.f;
       uint32_t pk[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2(s[2 * j] - m_new), p1 = ex2(s[2 * j + 1] - m_new);   // -inf -> 0
+        const float p0 = ex2(s[2 * j] - m_sub), p1 = ex2(s[2 * j + 1] - m_sub);   // -inf -> 0
         sum += p0 + p1;
         pk[j] = pack_bf16x2(p0, p1);
+        sum_bf += bf16_lo(pk[j]) + bf16_hi(pk[j]);    // the weights the PV MMA actually uses
       }
       l = l * alpha + sum;
+      l_bf = l_bf * alpha + sum_bf;
       m_run = m_new;
       // P buffer and O are free once the previous PV has completed
       if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (i - 1) & 1, abort_flag, p.status)))) break;
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (nblk - 1) & 1, abort_flag, p.status));
     tc_fence_after();
     if (ok) {
-      const float inv = 1.f / fmaxf(l, kSumexpFloor);
+      const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
       uint16_t* orow = p.out + ((int64_t)t * 128 + h) * kDv + 256 * crank;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {

@@ -221,6 +221,28 @@ def make_custom(T: int, H: int, topk: int, seqlens: list, seed: int, kind: str =
     return w
 
 
+def truncate(w: Workload, n_tokens: int) -> Workload:
+    """The first n_tokens tokens of a workload (a smaller case with the same
+    shapes per token): sequences are cut at n_tokens, and slots naming a row
+    at or past n_tokens become -1 padding."""
+    n = int(n_tokens)
+    lens, acc = [], 0
+    for L in w.seqlens:
+        if acc >= n:
+            break
+        lens.append(min(L, n - acc))
+        acc += lens[-1]
+    idx = np.array(w.indices[:n], copy=True)
+    idx[idx >= n] = -1
+    out = Workload(f"{w.name} (first {n} tokens)", n, w.H, w.topk, lens, w.scale, q_std=w.q_std, seed=w.seed)
+    out.indices = idx
+    out.cu_seqlens = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    out.q = None if w.q is None else w.q[:n]
+    out.kv = None if w.kv is None else w.kv[:n]
+    out.dout = None if w.dout is None else w.dout[:n]
+    return out
+
+
 def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
     """A fixed stratified row sample: every all-padding row (up to n/8), the
     first and last rows of every sequence (up to n/4), plus uniform rows."""
