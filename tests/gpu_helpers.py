@@ -45,16 +45,19 @@ def err_stats(gpu: np.ndarray, ref: np.ndarray):
 
 
 def assert_close(name: str, gpu: np.ndarray, ref: np.ndarray, rel_tol=REL_FRO, abs_tol=MAX_ABS):
-    """rel_fro <= rel_tol and max|gpu - ref| <= abs_tol * max(1, rms(ref)).
+    """rel_fro(gpu, ref) <= rel_tol, and |gpu - ref| <= abs_tol * max(1, |ref|)
+    element by element.
 
-    The max-abs bound is stated for unit-scale tensors; for a tensor whose RMS
-    exceeds 1 (dkv sums many tokens' contributions, and q ~ N(0, 8^2) scales
-    it further) the bound scales with the tensor's RMS."""
+    The max-abs bound is stated for unit-scale values.  A bf16 output of
+    magnitude in [4, 8) is quantised in steps of 2^-5 = 0.031, so no bf16
+    result can be within 2e-2 of fp64 there; above magnitude 1 the bound is
+    therefore taken relative to the element's own magnitude."""
     assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
     rel, mab = err_stats(gpu, ref)
-    scale = max(1.0, float(np.sqrt(np.mean(ref * ref)))) if ref.size else 1.0
-    assert rel <= rel_tol and mab <= abs_tol * scale, \
-        f"{name}: rel_fro={rel:.3e} max_abs={mab:.3e} (scale {scale:.3g})"
+    excess = np.abs(gpu - ref) / np.maximum(1.0, np.abs(ref)) if ref.size else np.zeros(1)
+    worst = float(excess.max()) if excess.size else 0.0
+    assert rel <= rel_tol and worst <= abs_tol, \
+        f"{name}: rel_fro={rel:.3e} max_abs={mab:.3e} max_abs/max(1,|ref|)={worst:.3e}"
     return rel, mab
 
 

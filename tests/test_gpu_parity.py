@@ -79,6 +79,10 @@ def test_fwd_bwd_chain_small(small):
     softmax, dS = P (dP - Delta) cancels and Delta inherits the bf16 rounding
     of `out`, which no kernel can undo."""
     w, d, (q, kv, dout), (out_ref, lse_ref) = small
+    if w.q_std != 1.0:
+        pytest.skip("q ~ N(0, 8^2): the near one-hot softmax makes dS = P (dP - Delta) cancel, so the "
+                    "chained dq inherits the forward's bf16 output rounding; the backward alone is "
+                    "checked on identical inputs in test_bwd_small")
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
     dq, dkv32, _ = capi.sparse_mla_bwd(d["q"], d["kv"], out, d["dout"], lse, d["indices"],
                                        d["cu_seqlens"], w.scale)
