@@ -43,6 +43,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_bwd_workspace_bytes.restype = S
     lib.sparse_mla_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, P, P, P, P, S, P]
     lib.sparse_mla_bwd.restype = I
+    lib.sparse_mla_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, P, P, P, P]
+    lib.sparse_mla_bwd_noalloc.restype = I
     lib.sparse_mla_check_indices.argtypes = [P, I, I, P, I, ctypes.POINTER(ctypes.c_int64), P]
     lib.sparse_mla_check_indices.restype = I
     lib.sparse_mla_last_error.argtypes = []
@@ -134,6 +136,29 @@ def sparse_mla_bwd(q, kv, out, dout, lse, indices, cu_seqlens, scale, dkv_mode=S
                                  _ptr(cu_seqlens), T, H, topk, B, float(scale), int(dkv_mode), _ptr(dq),
                                  _ptr(dkv_f32), _ptr(dkv), _ptr(workspace), workspace.numel(),
                                  _stream(stream)))
+    return dq, dkv_f32, dkv
+
+
+NOALLOC_MAX_ROWS = 1 << 23   # T * H limit of sparse_mla_bwd_noalloc
+
+
+def sparse_mla_bwd_noalloc(q, kv, out, dout, lse, indices, cu_seqlens, scale, dq=None, dkv_f32=None,
+                           dkv=None, want_bf16_dkv=True, stream=None):
+    """Backward that needs no workspace (the library keeps Delta in a fixed
+    device array, T*H <= 2^23).  Calls that overlap on the GPU race on that
+    array.  Output tensors may be passed in so that nothing is allocated."""
+    T, H, topk = _dims(q, indices)
+    dev = q.device
+    if dq is None:
+        dq = torch.empty((T, H, D_QK), dtype=torch.bfloat16, device=dev)
+    if dkv_f32 is None:
+        dkv_f32 = torch.empty((T, 1, D_QK), dtype=torch.float32, device=dev)
+    if dkv is None and want_bf16_dkv:
+        dkv = torch.empty((T, 1, D_QK), dtype=torch.bfloat16, device=dev)
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(load().sparse_mla_bwd_noalloc(_ptr(q), _ptr(kv), _ptr(out), _ptr(dout), _ptr(lse), _ptr(indices),
+                                         _ptr(cu_seqlens), T, H, topk, B, float(scale), _ptr(dq),
+                                         _ptr(dkv_f32), _ptr(dkv), _stream(stream)))
     return dq, dkv_f32, dkv
 
 

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <mutex>
 #include <string>
 
 #include "../../include/sparse_mla.h"
@@ -155,6 +156,94 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
   e = (H == 128) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
+  count_launches(1);
+  if (dkv != nullptr) {
+    e = smla::launch_cast_bf16(dkv_f32, dkv, (int64_t)T * smla::kDqk, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dkv cast launch");
+    count_launches(1);
+  }
+  return 0;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward entry point that allocates nothing.
+//
+// Some callers cannot call cudaMalloc at all: code that runs inside a memory
+// allocator's own callbacks (allocating there would re-enter the allocator),
+// and services whose device memory is fixed at start-up (they must not grow
+// or fragment it while serving).  sparse_mla_bwd needs its caller to hand it a
+// workspace for Delta; this variant keeps Delta in a fixed file-scope device
+// array instead, so the caller passes only inputs and outputs.
+namespace {
+
+constexpr size_t kNoAllocMaxRows = size_t(1) << 23;   // T * H <= 8,388,608 values (32 MiB of fp32)
+__device__ __align__(256) float g_noalloc_delta[kNoAllocMaxRows];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// In host code g_noalloc_delta names a host-side stand-in, not the device
+// array, so its device address is looked up once per device (with that device
+// current) and cached.  This is the only set-up step.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(-ENOTSUP, "device %d is beyond the %d devices the no-allocation path tracks", dev,
+                kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_delta);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                           const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                           const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                           smla_bf16_t* dq, float* dkv_f32, smla_bf16_t* dkv, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  if ((size_t)T * (size_t)H > kNoAllocMaxRows)
+    return fail(-EINVAL, "T*H = %lld exceeds the no-allocation scratch limit of %zu (T*H values)",
+                (long long)T * H, kNoAllocMaxRows);
+  if (T == 0) return 0;
+  SMLA_REQUIRE_PTR(q);
+  SMLA_REQUIRE_PTR(kv);
+  SMLA_REQUIRE_PTR(out);
+  SMLA_REQUIRE_PTR(dout);
+  SMLA_REQUIRE_PTR(lse);
+  SMLA_REQUIRE_PTR(indices);
+  SMLA_REQUIRE_PTR(dq);
+  SMLA_REQUIRE_PTR(dkv_f32);
+  if (dkv != nullptr && !aligned16(dkv)) return fail(-EINVAL, "dkv must be 16-byte aligned");
+  if (int r = check_device()) return r;
+  float* delta = nullptr;
+  if (int r = noalloc_scratch(&delta)) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Delta is fully rewritten here before the backward kernel reads it.
+  cudaError_t e = smla::launch_delta(out, dout, delta, (int64_t)T * H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "delta launch");
+  count_launches(1);
+  e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
+  smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
+  e = (H == 128) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd_noalloc launch");
   count_launches(1);
   if (dkv != nullptr) {
     e = smla::launch_cast_bf16(dkv_f32, dkv, (int64_t)T * smla::kDqk, s);

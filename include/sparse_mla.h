@@ -115,6 +115,32 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward that allocates nothing (the pages have no counterpart: this is an
+ * interface addition for callers that cannot call cudaMalloc: code running
+ * inside a memory allocator's own callbacks, where allocating would re-enter
+ * the allocator, and services whose device memory is fixed at start-up).
+ *
+ * Same arguments, results and error codes as sparse_mla_bwd with
+ * dkv_mode = SMLA_DKV_ATOMIC, minus the workspace: the Delta scratch lives in
+ * a fixed device array inside the library, 2^23 fp32 values (32 MiB), which
+ * every GPU that loads the library holds until the process exits.
+ *   - T * H must be <= 8,388,608 (e.g. T = 65536 at H = 128); larger sizes
+ *     return -EINVAL with a message and launch nothing.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call on each device (with that device current) looks up the device
+ *     address of the array once; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (each call rewrites the part it uses before reading it).  Calls that
+ *     overlap on the GPU -- on different streams, or from different host
+ *     threads -- race on it and must be serialised by the caller.
+ */
+int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                           const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                           const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                           smla_bf16_t* dq, float* dkv_f32, smla_bf16_t* dkv, void* stream);
+
+/*
  * Index validation (Megatron-Bridge PR #17, Bug fixes: top-k padded with
  * -1).  Counts the entries of indices [T, 1, topk] that are neither -1 nor a
  * row of their own query's sequence [cu_seqlens[b], cu_seqlens[b+1]).
