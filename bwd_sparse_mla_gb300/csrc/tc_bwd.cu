@@ -8,17 +8,20 @@
 // dims) in TMEM, and produces its slice of every dKV row.
 //
 // Per block of 32 top-k slots:
-//   producer : masked TMA gather4 of the CTA's columns of the 32 named rows
-//              (padding slots read an out-of-range row: exact zeros);
+//   producer : masked 16-byte cp.async gather of the CTA's columns of the 32
+//              named rows, indices read one block ahead (padding slots copy
+//              zero bytes: exact-zero K/V rows);
 //   MMA      : S_half = q_half K_half^T and dP_half = dO_half V_half^T
 //              (M=128 heads, N=32 slots) into TMEM;
-//   softmax  : one thread per head swaps its partial S and dP rows with the
-//              peer CTA through distributed shared memory, sums them
+//   softmax  : one thread per head sends its partial S and dP rows to the
+//              peer CTA with st.async, sums them with the peer's partials
 //              (both CTAs obtain bit-identical sums), recomputes
 //              P = exp2(S*scale*log2e - lse*log2e) (0 on padding slots),
-//              dS' = scale * P * (dP - Delta), and stores P and dS' as bf16;
-//   MMA      : dQ_half += dS' K_half (M=128, N=256|320, K=32) and the
-//              transposed dKV tiles dKV^T[d, j] = dO^T P + q^T dS'
+//              dS' = scale * P * (dP - Delta), and stores P as bf16 and dS'
+//              as a bf16 pair hi + lo (dS' - hi rounded again), so the dQ and
+//              dKV products see dS' to about 16 bits;
+//   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
+//              transposed dKV tiles dKV^T[d, j] = dO^T P + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
 //   drain    : four warps read the dKV tiles from TMEM and add them into the
 //              fp32 dKV rows named by the valid slots (coalesced 128-byte
@@ -35,7 +38,11 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 32;
-constexpr int kThreads = 320;           // w0 producer, w1 MMA, w2..5 softmax, w6..9 dKV drain
+constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax, w7..10 dKV drain
+constexpr int kMmaWarp = 2;
+constexpr int kDrainWarp0 = 7;
+constexpr int kThreads = 352;
+constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4
 constexpr int kChunk = 128 * 128;       // 64-dim chunk of q / dO for 128 heads
 constexpr int kChunkKV = kBK * 128;     // 64-dim chunk of a 32-row KV block
 constexpr int kStage = 5 * kChunkKV;
@@ -46,16 +53,18 @@ constexpr int SM_DO = SM_Q + 5 * kChunk;                // 4 chunks
 constexpr int SM_KV = SM_DO + 4 * kChunk;               // 2 stages
 constexpr int SM_X = SM_KV + 2 * kStage;                // exchange rows, then P / dS
 constexpr int SM_P = SM_X;                              // 128 rows x 64 B, 64B swizzle
-constexpr int SM_DS = SM_X + 128 * 64;
+constexpr int SM_DS = SM_X + 128 * 64;                 // dS' hi
+constexpr int SM_DSLO = SM_X + 2 * 128 * 64;            // dS' lo
 constexpr int SM_ROWS = SM_X + 128 * kXPitch;           // 2 x 32 int32
 constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
 constexpr int SM_BAR = SM_MASK + 8;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 8,
-           P_FULL = 9, PDS_FREE = 10, DKV_FULL = 11, DKV_FREE = 12, NBAR = 13 };
+           P_FULL = 9, PDS_FREE = 10, DKV_FULL = 11, DKV_FREE = 12, X_READ = 13, NBAR = 14 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_ABORT = SM_TMEM + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;
 static_assert(SM_X % 1024 == 0, "swizzle atoms");
+static_assert(SM_DSLO + 128 * 64 <= SM_X + 128 * kXPitch, "P / dS' hi / dS' lo fit in the exchange area");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
@@ -65,6 +74,7 @@ constexpr uint32_t TM_DP = 352;         // 32
 constexpr uint32_t TM_DKV = 384;        // up to 3 tiles x 32
 
 struct TcBwdParams {
+  const uint16_t* kv;
   const int32_t* indices;
   const float* lse;
   const float* delta;
@@ -78,8 +88,8 @@ struct TcBwdParams {
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
-    tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_do, TcBwdParams p) {
+    tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       TcBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
@@ -96,22 +106,24 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar_addr(sb, KV_FULL + 0), 1);
-    mbar_init(bar_addr(sb, KV_FULL + 1), 1);
+    mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + mask/rows
+    mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
     mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 128);   // MMA commit + drain threads (row list read)
     mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 128);
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FREE), 128);
-    mbar_init(bar_addr(sb, X_FULL), 128);
-    mbar_init(bar_addr(sb, X_EMPTY), 128);
+    mbar_init(bar_addr(sb, X_FULL), 1);     // armed with the bytes the peer sends
+    mbar_init(bar_addr(sb, X_EMPTY), 1);    // the peer's exchange area is free and armed
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
     mbar_init(bar_addr(sb, DKV_FREE), 128);
+    mbar_init(bar_addr(sb, X_READ), 128);
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);   // block 0's partials from the peer
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sb + SM_TMEM, kTmemCols);
     tmem_relinquish();
   }
@@ -121,11 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < kProducers / 32) {
+    // ------------------------------------------------------------ producers
+    const int pt = threadIdx.x;              // 0..63
+    if (pt == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kv);
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (nch + 4) * kChunk);
       for (int k = 0; k < nch; ++k)
@@ -133,35 +145,52 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       for (int k = 0; k < 4; ++k)
         tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
     }
+    // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
+    const int c16 = pt & 7, r0 = pt >> 3;
+    constexpr int RS = kProducers / 8;
     const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    const uint16_t* kvc = p.kv + 64 * g0 + 8 * c16;
     int* srows = reinterpret_cast<int*>(smem + SM_ROWS);
+    int nxt[kRowsPerProducer], nm = 0;
+#pragma unroll
+    for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + r0 + RS * j);
+    if (warp == 0) nm = __ldg(irow + lane);
     for (int i = 0; i < nblk; ++i) {
       const int st = i & 1;
-      int ok = 1;
-      if (i >= 2 && lane == 0) ok = mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.status);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int a = __ldg(irow + i * kBK + lane);
-      const bool va = (a >= 0 && a < p.T);
-      const int ra = va ? a : p.T;         // out-of-range row: TMA fills zeros
-      const uint32_t m = __ballot_sync(0xffffffffu, va);
-      srows[st * 32 + lane] = va ? a : -1;
-      __syncwarp();
-      if (lane == 0) {
-        *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st) = m;
-        mbar_arrive_expect_tx(bar_addr(sb, KV_FULL + st), nch * kChunkKV);
-      }
-      __syncwarp();
-      int rows[4];
+      int cur[kRowsPerProducer];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) rows[k] = __shfl_sync(0xffffffffu, ra, (4 * (lane & 7) + k) & 31);
-      if (lane < 8) {
-        const uint32_t dst = sb + SM_KV + st * kStage + lane * 4 * 128;
-        for (int k = 0; k < nch; ++k)
-          tma_gather4(dst + k * kChunkKV, &tm_kv, 64 * (g0 + k), rows[0], rows[1], rows[2], rows[3],
-                      bar_addr(sb, KV_FULL + st));
+      for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
+      const int cm = nm;
+      if (i + 1 < nblk) {                    // indices of the next block, one block ahead
+#pragma unroll
+        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + (i + 1) * kBK + r0 + RS * j);
+        if (warp == 0) nm = __ldg(irow + (i + 1) * kBK + lane);
+      }
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag,
+                                                       p.status)))
+        break;                                 // warp-uniform exit
+      const uint32_t stage = sb + SM_KV + st * kStage;
+#pragma unroll
+      for (int j = 0; j < kRowsPerProducer; ++j) {
+        const int r = r0 + RS * j;
+        const bool v = cur[j] >= 0 && cur[j] < p.T;
+        const uint16_t* src = kvc + (int64_t)(v ? cur[j] : 0) * kDqk;
+        const uint32_t dst = stage + r * 128 + ((c16 ^ (r & 7)) << 4);
+        for (int k = 0; k < nch; ++k) cp_async16(dst + k * kChunkKV, src + 64 * k, v ? 16u : 0u);
+      }
+      cp_async_arrive(bar_addr(sb, KV_FULL + st));
+      if (warp == 0) {                        // slot mask and row list of the block
+        const bool v = cm >= 0 && cm < p.T;
+        const uint32_t m = __ballot_sync(0xffffffffu, v);
+        srows[st * 32 + lane] = v ? cm : -1;
+        __syncwarp();
+        if (lane == 0) {
+          *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st) = m;
+          mbar_arrive(bar_addr(sb, KV_FULL + st));
+        }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_sdp = idesc_bf16(128, kBK, false, false);
@@ -177,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const uint32_t kvb = sb + SM_KV + st * kStage;
           if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
           if (i >= 1 && !(ok = mbar_wait(bar_addr(sb, SDP_FREE), (i - 1) & 1, abort_flag, p.status))) break;
+          fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
           // S_half = q_half K_half^T ; dP_half = dO_half V_half^T   (K-major operands, 128B swizzle)
           for (int k = 0; k < nch; ++k)
@@ -196,15 +226,19 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const uint32_t kvb = sb + SM_KV + stj * kStage;
           if (!(ok = mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status))) break;
           tc_fence_after();
-          // dQ_half += dS' K_half: A = dS' (K-major, 64B swizzle), B = K block read MN-major
+          // dQ_half += (hi + lo) K_half: A = dS' (K-major, 64B swizzle), B = K block read MN-major
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = sdesc_sw64(sb + SM_DS + ks * 32, 16, 512);
-            mma_bf16_ss(tmem + TM_DQ, ad, sdesc_sw128(kvb + ks * 16 * 128, kChunkKV, 1024), id_dq256,
-                        (j > 0 || ks > 0));
-            if (nch == 5)
-              mma_bf16_ss(tmem + TM_DQ + 256, ad, sdesc_sw128(kvb + 4 * kChunkKV + ks * 16 * 128, kChunkKV, 1024),
-                          id_dq64, (j > 0 || ks > 0));
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t dsb = part == 0 ? SM_DS : SM_DSLO;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t ad = sdesc_sw64(sb + dsb + ks * 32, 16, 512);
+              const uint32_t acc = (j > 0 || part > 0 || ks > 0);
+              mma_bf16_ss(tmem + TM_DQ, ad, sdesc_sw128(kvb + ks * 16 * 128, kChunkKV, 1024), id_dq256, acc);
+              if (nch == 5)
+                mma_bf16_ss(tmem + TM_DQ + 256, ad,
+                            sdesc_sw128(kvb + 4 * kChunkKV + ks * 16 * 128, kChunkKV, 1024), id_dq64, acc);
+            }
           }
           // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
           //   dKV^T = q_half^T dS' + dO_half^T P   (A MN-major 128B swizzle, B MN-major 64B swizzle)
@@ -213,9 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           for (int m = 0; m < ntile; ++m) {
             const uint32_t d_t = tmem + TM_DKV + 32 * m;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_bf16_ss(d_t, sdesc_sw128(sb + SM_Q + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024),
-                          sdesc_sw64(sb + SM_DS + ks * 16 * 64, 8192, 512), id_dkv, ks != 0);
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = sdesc_sw128(sb + SM_Q + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024);
+              mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_DS + ks * 16 * 64, 8192, 512), id_dkv, ks != 0);
+              mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_DSLO + ks * 16 * 64, 8192, 512), id_dkv, 1);
+            }
             if (2 * m < 4) {   // tiles inside the value range also get the dO^T P term
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
@@ -230,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < kDrainWarp0) {
     // ------------------------------------------------------------ softmax / dS
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
@@ -243,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const float dl = p.delta[(int64_t)t * 128 + h];
     uint8_t* prow = smem + SM_P + h * 64;
     uint8_t* dsrow = smem + SM_DS + h * 64;
+    uint8_t* dlrow = smem + SM_DSLO + h * 64;
     const int sw = (h >> 1) & 3;        // 64B swizzle: 16-byte chunk index ^= address bits [7,9)
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
@@ -255,18 +292,26 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, SDP_FREE));
       if (i >= 1) {
-        // this CTA's MMAs are done with its P / dS (which live in its exchange rows):
-        // let the peer write the next partial rows here
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status)))) break;
-        mbar_arrive_remote(xempty_peer);
+        // once this CTA's MMAs are done with P / dS' (which live in its exchange
+        // area), re-arm the area and let the peer send the next partial rows
+        int okx = 1;
+        if (h == 0) {
+          okx = mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status);
+          if (okx) {
+            mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);
+            mbar_arrive_remote(xempty_peer);
+          }
+        }
+        if (!(ok = __all_sync(0xffffffffu, okx))) break;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
       }
-#pragma unroll
-      for (int v = 0; v < 8; ++v) st_cluster_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+      // partial rows to the peer: st.async counts the bytes on the peer's X_FULL
 #pragma unroll
       for (int v = 0; v < 8; ++v)
-        st_cluster_v4(xrow_peer + 128 + 16 * v, dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
-      mbar_arrive_remote(xfull_peer);
+        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        st_async_v4(xrow_peer + 128 + 16 * v, dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3], xfull_peer);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
       const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
 #pragma unroll
@@ -275,22 +320,28 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
         dp[4 * v] += b.x; dp[4 * v + 1] += b.y; dp[4 * v + 2] += b.z; dp[4 * v + 3] += b.w;
       }
-      named_bar(1, 128);   // every exchange row is read before P / dS overwrite the area
+      // every exchange row is read before P / dS' overwrite the area
+      mbar_arrive(bar_addr(sb, X_READ));
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, X_READ), i & 1, abort_flag, p.status)))) break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
-      uint32_t pp[16], dd[16];
+      uint32_t pp[16], dd[16], dl2[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
         const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
         const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
         pp[j] = pack_bf16x2(p0, p1);
-        dd[j] = pack_bf16x2(p.scale * p0 * (dp[2 * j] - dl), p.scale * p1 * (dp[2 * j + 1] - dl));
+        const float d0 = p.scale * p0 * (dp[2 * j] - dl), d1 = p.scale * p1 * (dp[2 * j + 1] - dl);
+        dd[j] = pack_bf16x2(d0, d1);
+        dl2[j] = pack_bf16x2(d0 - bf16_lo(dd[j]), d1 - bf16_hi(dd[j]));   // the part bf16 dropped
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
         *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
+        *reinterpret_cast<uint4*>(dlrow + ((c ^ sw) << 4)) =
+            make_uint4(dl2[4 * c], dl2[4 * c + 1], dl2[4 * c + 2], dl2[4 * c + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -351,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -391,16 +442,15 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 uint32_t* tc_status_ptr();
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
-  CUtensorMap tm_q, tm_kv, tm_do;
+  CUtensorMap tm_q, tm_do;
   if (!make_map(&tm_q, a.q, kDqk, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&tm_kv, a.kv, kDqk, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
   if (!make_map(&tm_do, a.dout, kDv, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
   uint32_t* status = tc_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  TcBwdParams p{a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
-  tc_bwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_kv, tm_do, p);
+  TcBwdParams p{a.kv, a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
+  tc_bwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }
 

@@ -11,15 +11,18 @@
 // scores and take identical softmax decisions).
 //
 // Per block of 64 top-k slots:
-//   producer warp : reads the 64 indices, masks them (valid iff 0 <= idx < T),
-//                   and gathers the rows with TMA gather4 into 128B-swizzled
-//                   shared memory; padding slots use an out-of-range row, so
-//                   TMA fills them with zeros (exact-zero K and V, as in the
-//                   miles PR #2079 fix, implementation breakdown item 2);
+//   producer warps: read the 64 indices (one block ahead), mask them (valid
+//                   iff 0 <= idx < T) and gather this CTA's columns of the
+//                   named rows with 16-byte cp.async into 128B-swizzled shared
+//                   memory; a padding slot copies zero bytes and gets an
+//                   exact-zero K/V row (the clamp + mask of the miles PR #2079
+//                   fix, implementation breakdown item 2);
 //   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
 //                   into TMEM, then O += P V_half (M=128, N=256, K=64);
-//   softmax warps : one thread per head: load the 64 partial scores, swap
-//                   halves with the peer CTA, mask padding to -inf, online
+//   softmax warps : one thread per head: load the 64 partial scores, send
+//                   them to the peer CTA with st.async (which signals the
+//                   peer's mbarrier as the bytes land), add the peer's
+//                   partials, mask padding to -inf, online
 //                   softmax in the exp2 domain with a lazily updated running
 //                   max, rescale O in TMEM when the max moves, write P (bf16)
 //                   for the PV MMA.  At the end the sum of exponentials is
@@ -36,7 +39,10 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA, warps 2..5 softmax
+constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax
+constexpr int kMmaWarp = 2;
+constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
+constexpr int kThreads = kProducers + 32 + 128;
 constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
@@ -51,7 +57,7 @@ constexpr int SM_X = SM_P + 128 * 128;
 constexpr int SM_MASK = SM_X + 128 * kXPitch;       // 2 x u64
 constexpr int SM_BAR = SM_MASK + 16;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 10,
-           P_FULL = 11, O_DONE = 12, NBAR = 13 };
+           P_FULL = 11, O_DONE = 12, X_READ = 13, NBAR = 14 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_ABORT = SM_TMEM + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;     // + alignment slack
@@ -62,6 +68,7 @@ constexpr uint32_t TM_O = 0;            // 256 columns
 constexpr uint32_t TM_S = 256;          // 2 x 64 columns
 
 struct TcFwdParams {
+  const uint16_t* kv;                   // [T, 576] bf16
   const int32_t* indices;
   uint16_t* out;
   float* lse;
@@ -73,8 +80,7 @@ struct TcFwdParams {
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
-    tc_fwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                       TcFwdParams p) {
+    tc_fwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, TcFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned (128B swizzle atoms)
   const uint32_t sb = smem_u32(smem);
@@ -89,8 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar_addr(sb, KV_FULL + 0), 1);
-    mbar_init(bar_addr(sb, KV_FULL + 1), 1);
+    mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + the slot mask
+    mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
     mbar_init(bar_addr(sb, KV_EMPTY + 0), 1);
     mbar_init(bar_addr(sb, KV_EMPTY + 1), 1);
     mbar_init(bar_addr(sb, Q_FULL), 1);
@@ -98,13 +104,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
     mbar_init(bar_addr(sb, S_FREE + 0), 128);
     mbar_init(bar_addr(sb, S_FREE + 1), 128);
-    mbar_init(bar_addr(sb, X_FULL), 128);       // arrivals from the peer's 128 softmax threads
-    mbar_init(bar_addr(sb, X_EMPTY), 128);
+    mbar_init(bar_addr(sb, X_FULL), 1);         // armed here with the bytes the peer sends
+    mbar_init(bar_addr(sb, X_EMPTY), 1);        // the peer has read our partials and re-armed
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, O_DONE), 1);
+    mbar_init(bar_addr(sb, X_READ), 128);       // all softmax threads have read the peer's partials
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);   // block 0's partial scores from the peer
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sb + SM_TMEM, kTmemCols);
     tmem_relinquish();
   }
@@ -114,49 +122,58 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < kProducers / 32) {
+    // ------------------------------------------------------------ producers
+    const int pt = threadIdx.x;              // 0..63
+    if (pt == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kv);
       mbar_arrive_expect_tx(bar_addr(sb, Q_FULL), nch * kChunkQ);
       for (int k = 0; k < nch; ++k)
         tma_load_2d(sb + SM_Q + k * kChunkQ, &tm_q, 64 * (g0 + k), t * 128, bar_addr(sb, Q_FULL));
     }
+    // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
+    const int c16 = pt & 7, r0 = pt >> 3;
+    constexpr int RS = kProducers / 8;       // row stride between a thread's rows
     const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    const uint16_t* kvc = p.kv + 64 * g0 + 8 * c16;
+    int nxt[kRowsPerProducer], nm[2];
+#pragma unroll
+    for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + r0 + RS * j);
+    if (warp == 0) { nm[0] = __ldg(irow + lane); nm[1] = __ldg(irow + 32 + lane); }
     for (int i = 0; i < nblk; ++i) {
       const int st = i & 1;
-      int ok = 1;
-      if (i >= 2 && lane == 0) ok = mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.status);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // warp-uniform exit
-      const int a = __ldg(irow + i * kBK + lane);
-      const int b = __ldg(irow + i * kBK + 32 + lane);
-      const bool va = (a >= 0 && a < p.T), vb = (b >= 0 && b < p.T);
-      const int ra = va ? a : p.T;      // row T is out of range: TMA fills zeros
-      const int rb = vb ? b : p.T;
-      const uint32_t ma = __ballot_sync(0xffffffffu, va), mbk = __ballot_sync(0xffffffffu, vb);
-      if (lane == 0) {
-        *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st) = (uint64_t)ma | ((uint64_t)mbk << 32);
-        mbar_arrive_expect_tx(bar_addr(sb, KV_FULL + st), nch * kChunkKV);
-      }
-      __syncwarp();
-      // lane g < 16 gathers slots 4g .. 4g+3
-      int rows[4];
+      int cur[kRowsPerProducer], cm[2];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int slot = 4 * (lane & 15) + k;
-        const int xa = __shfl_sync(0xffffffffu, ra, slot & 31);
-        const int xb = __shfl_sync(0xffffffffu, rb, slot & 31);
-        rows[k] = slot < 32 ? xa : xb;
+      for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
+      cm[0] = nm[0]; cm[1] = nm[1];
+      if (i + 1 < nblk) {                    // indices of the next block, one block ahead
+#pragma unroll
+        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + (i + 1) * kBK + r0 + RS * j);
+        if (warp == 0) { nm[0] = __ldg(irow + (i + 1) * kBK + lane); nm[1] = __ldg(irow + (i + 1) * kBK + 32 + lane); }
       }
-      if (lane < 16) {
-        const uint32_t dst = sb + SM_KV + st * kStageBytes + lane * 4 * 128;
-        for (int k = 0; k < nch; ++k)
-          tma_gather4(dst + k * kChunkKV, &tm_kv, 64 * (g0 + k), rows[0], rows[1], rows[2], rows[3],
-                      bar_addr(sb, KV_FULL + st));
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag,
+                                                       p.status)))
+        break;                                 // warp-uniform exit
+      const uint32_t stage = sb + SM_KV + st * kStageBytes;
+#pragma unroll
+      for (int j = 0; j < kRowsPerProducer; ++j) {
+        const int r = r0 + RS * j;
+        const bool v = cur[j] >= 0 && cur[j] < p.T;
+        const uint16_t* src = kvc + (int64_t)(v ? cur[j] : 0) * kDqk;
+        const uint32_t dst = stage + r * 128 + ((c16 ^ (r & 7)) << 4);
+        for (int k = 0; k < nch; ++k) cp_async16(dst + k * kChunkKV, src + 64 * k, v ? 16u : 0u);
+      }
+      cp_async_arrive(bar_addr(sb, KV_FULL + st));
+      if (warp == 0) {                        // slot validity mask of the block for the softmax warps
+        const uint32_t ma = __ballot_sync(0xffffffffu, cm[0] >= 0 && cm[0] < p.T);
+        const uint32_t mb = __ballot_sync(0xffffffffu, cm[1] >= 0 && cm[1] < p.T);
+        if (lane == 0) {
+          *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st) = (uint64_t)ma | ((uint64_t)mb << 32);
+          mbar_arrive(bar_addr(sb, KV_FULL + st));
+        }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
@@ -167,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const int st = i & 1, b = i & 1;
           if (!mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)) break;
           if (i >= 2 && !mbar_wait(bar_addr(sb, S_FREE + b), ((i - 2) >> 1) & 1, abort_flag, p.status)) break;
+          fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
           for (int k = 0; k < nch; ++k) {
 #pragma unroll
@@ -218,11 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_ld64(tl + TM_S + 64 * b, s);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_FREE + b));
-      // swap partial scores with the peer CTA
+      // send the partial scores to the peer (st.async lands them and counts the
+      // bytes on the peer's X_FULL), then take the peer's partials
       if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
 #pragma unroll
-      for (int v = 0; v < 16; ++v) st_cluster_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-      mbar_arrive_remote(xfull_peer);
+      for (int v = 0; v < 16; ++v)
+        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
       const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
 #pragma unroll
@@ -230,7 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         const float4 o = xr[v];
         s[4 * v] += o.x; s[4 * v + 1] += o.y; s[4 * v + 2] += o.z; s[4 * v + 3] += o.w;
       }
-      mbar_arrive_remote(xempty_peer);
+      mbar_arrive(bar_addr(sb, X_READ));
+      int okx = 1;
+      if (h == 0) {                            // once all rows are read: re-arm, then let the peer send
+        okx = mbar_wait(bar_addr(sb, X_READ), i & 1, abort_flag, p.status);
+        if (okx) {
+          mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);
+          mbar_arrive_remote(xempty_peer);
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, okx))) break;
       // slot validity of this block (written by the producer before it armed KV_FULL)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
@@ -306,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // the peer no longer touches this CTA's shared memory
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -362,15 +390,14 @@ cudaError_t read_tc_status(uint32_t* out, bool clear) {
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q;
   if (!make_map_576(&tm_q, a.q, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
-  if (!make_map_576(&tm_kv, a.kv, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
   uint32_t* status = tc_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  TcFwdParams p{a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
-  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_kv, p);
+  TcFwdParams p{a.kv, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
+  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, p);
   return cudaGetLastError();
 }
 
