@@ -17,11 +17,11 @@
 //              peer CTA with st.async, sums them with the peer's partials
 //              (both CTAs obtain bit-identical sums), recomputes
 //              P = exp2(S*scale*log2e - lse*log2e) (0 on padding slots),
-//              dS' = scale * P * (dP - Delta), and stores P as bf16 and dS'
-//              as a bf16 pair hi + lo (dS' - hi rounded again), so the dQ and
-//              dKV products see dS' to about 16 bits;
+//              dS' = scale * P * (dP - Delta), and stores P and dS' each as
+//              a bf16 pair hi + lo (x - hi rounded again), so the dQ and dKV
+//              products see them to about 16 significant bits;
 //   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
-//              transposed dKV tiles dKV^T[d, j] = dO^T P + q^T (hi + lo)
+//              transposed dKV tiles dKV^T[d, j] = dO^T (hi + lo) + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
 //   drain    : four warps read the dKV tiles from TMEM and add them into the
 //              fp32 dKV rows named by the valid slots (coalesced 128-byte
@@ -55,6 +55,7 @@ constexpr int SM_X = SM_KV + 2 * kStage;                // exchange rows, then P
 constexpr int SM_P = SM_X;                              // 128 rows x 64 B, 64B swizzle
 constexpr int SM_DS = SM_X + 128 * 64;                 // dS' hi
 constexpr int SM_DSLO = SM_X + 2 * 128 * 64;            // dS' lo
+constexpr int SM_PLO = SM_X + 3 * 128 * 64;             // P lo
 constexpr int SM_ROWS = SM_X + 128 * kXPitch;           // 2 x 32 int32
 constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
 constexpr int SM_BAR = SM_MASK + 8;
@@ -64,7 +65,7 @@ constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_ABORT = SM_TMEM + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;
 static_assert(SM_X % 1024 == 0, "swizzle atoms");
-static_assert(SM_DSLO + 128 * 64 <= SM_X + 128 * kXPitch, "P / dS' hi / dS' lo fit in the exchange area");
+static_assert(SM_PLO + 128 * 64 <= SM_X + 128 * kXPitch, "P, dS' (hi and lo) and P lo fit in the exchange area");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
@@ -255,8 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             if (2 * m < 4) {   // tiles inside the value range also get the dO^T P term
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ss(d_t, sdesc_sw128(sb + SM_DO + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024),
-                            sdesc_sw64(sb + SM_P + ks * 16 * 64, 8192, 512), id_dkv, 1);
+              {
+                const uint64_t ad = sdesc_sw128(sb + SM_DO + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024);
+                mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_P + ks * 16 * 64, 8192, 512), id_dkv, 1);
+                mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_PLO + ks * 16 * 64, 8192, 512), id_dkv, 1);
+              }
             }
           }
           mma_commit(bar_addr(sb, DKV_FULL));
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     uint8_t* prow = smem + SM_P + h * 64;
     uint8_t* dsrow = smem + SM_DS + h * 64;
     uint8_t* dlrow = smem + SM_DSLO + h * 64;
+    uint8_t* plrow = smem + SM_PLO + h * 64;
     const int sw = (h >> 1) & 3;        // 64B swizzle: 16-byte chunk index ^= address bits [7,9)
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
@@ -325,13 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, X_READ), i & 1, abort_flag, p.status)))) break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
-      uint32_t pp[16], dd[16], dl2[16];
+      uint32_t pp[16], dd[16], dl2[16], pl[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
         const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
         const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
         pp[j] = pack_bf16x2(p0, p1);
+        pl[j] = pack_bf16x2(p0 - bf16_lo(pp[j]), p1 - bf16_hi(pp[j]));
         const float d0 = p.scale * p0 * (dp[2 * j] - dl), d1 = p.scale * p1 * (dp[2 * j + 1] - dl);
         dd[j] = pack_bf16x2(d0, d1);
         dl2[j] = pack_bf16x2(d0 - bf16_lo(dd[j]), d1 - bf16_hi(dd[j]));   // the part bf16 dropped
@@ -342,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
         *reinterpret_cast<uint4*>(dlrow + ((c ^ sw) << 4)) =
             make_uint4(dl2[4 * c], dl2[4 * c + 1], dl2[4 * c + 2], dl2[4 * c + 3]);
+        *reinterpret_cast<uint4*>(plrow + ((c ^ sw) << 4)) = make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();

@@ -19,10 +19,12 @@
 //                   fix, implementation breakdown item 2);
 //   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
 //                   into TMEM, then O += P V_half (M=128, N=256, K=64);
-//   softmax warps : one thread per head: load the 64 partial scores, send
+//   sender warps  : one thread per head: load the 64 partial scores and send
 //                   them to the peer CTA with st.async (which signals the
-//                   peer's mbarrier as the bytes land), add the peer's
-//                   partials, mask padding to -inf, online
+//                   peer's mbarrier as the bytes land), one block ahead of
+//                   the softmax warps, so the exchange overlaps the softmax;
+//   softmax warps : one thread per head: load the 64 partial scores, add the
+//                   peer's partials, mask padding to -inf, online
 //                   softmax in the exp2 domain with a lazily updated running
 //                   max, rescale O in TMEM when the max moves, write P (bf16)
 //                   for the PV MMA.  At the end the sum of exponentials is
@@ -39,10 +41,11 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax
+constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax, 7..10 senders
 constexpr int kMmaWarp = 2;
+constexpr int kSenderWarp0 = 7;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
-constexpr int kThreads = kProducers + 32 + 128;
+constexpr int kThreads = kProducers + 32 + 128 + 128;
 constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
@@ -102,8 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, Q_FULL), 1);
     mbar_init(bar_addr(sb, S_FULL + 0), 1);
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
-    mbar_init(bar_addr(sb, S_FREE + 0), 128);
-    mbar_init(bar_addr(sb, S_FREE + 1), 128);
+    mbar_init(bar_addr(sb, S_FREE + 0), 256);   // softmax and sender threads have read the scores
+    mbar_init(bar_addr(sb, S_FREE + 1), 256);
     mbar_init(bar_addr(sb, X_FULL), 1);         // armed here with the bytes the peer sends
     mbar_init(bar_addr(sb, X_EMPTY), 1);        // the peer has read our partials and re-armed
     mbar_init(bar_addr(sb, P_FULL), 128);
@@ -214,14 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSenderWarp0) {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int h = 32 * q4 + lane;            // head == TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xrow = sb + SM_X + h * kXPitch;
-    const uint32_t xrow_peer = mapa(xrow, peer);
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
     uint8_t* prow = smem + SM_P + h * 128;
     // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
@@ -236,12 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_ld64(tl + TM_S + 64 * b, s);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_FREE + b));
-      // send the partial scores to the peer (st.async lands them and counts the
-      // bytes on the peer's X_FULL), then take the peer's partials
-      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
-#pragma unroll
-      for (int v = 0; v < 16; ++v)
-        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
+      // the peer's partial scores for this block (sent by its sender warps)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
       const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
 #pragma unroll
@@ -292,12 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_after();
       if (i >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
-        for (int part = 0; part < 4; ++part) {
-          float o[64];
-          tmem_ld64(tl + TM_O + 64 * part, o);
+        for (int part = 0; part < 8; ++part) {
+          float o[32];
+          tmem_ld32(tl + TM_O + 32 * part, o);
 #pragma unroll
-          for (int j = 0; j < 64; ++j) o[j] *= alpha;
-          tmem_st64(tl + TM_O + 64 * part, o);
+          for (int j = 0; j < 32; ++j) o[j] *= alpha;
+          tmem_st32(tl + TM_O + 32 * part, o);
         }
         tmem_wait_st();
       }
@@ -316,16 +311,38 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
       uint16_t* orow = p.out + ((int64_t)t * 128 + h) * kDv + 256 * crank;
 #pragma unroll 1
-      for (int part = 0; part < 4; ++part) {
-        float o[64];
-        tmem_ld64(tl + TM_O + 64 * part, o);
-        uint4* dst = reinterpret_cast<uint4*>(orow + 64 * part);
+      for (int part = 0; part < 8; ++part) {
+        float o[32];
+        tmem_ld32(tl + TM_O + 32 * part, o);
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * part);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                               pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
       }
       if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
+    }
+    } else {
+    // ------------------------------------------------------------ senders
+    const int q4 = warp & 3;
+    const int h = 32 * q4 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xrow_peer = mapa(sb + SM_X + h * kXPitch, peer);
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    for (int i = 0; i < nblk; ++i) {
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (i >> 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      float s[64];
+      tmem_ld64(tl + TM_S + 64 * b, s);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, S_FREE + b));
+      // the peer has read the previous block's partials and re-armed its X_FULL
+      if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))
+        break;
+#pragma unroll
+      for (int v = 0; v < 16; ++v)
+        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
     }
   }
 
