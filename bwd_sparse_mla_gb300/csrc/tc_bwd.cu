@@ -198,47 +198,58 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const uint32_t id_dq256 = idesc_bf16(128, 256, false, true);
       const uint32_t id_dq64 = idesc_bf16(128, 64, false, true);
       const uint32_t id_dkv = idesc_bf16(128, kBK, true, true);
+      // base descriptors; per-MMA descriptors only move the start address
+      const uint64_t dq0 = sdesc_sw128(sb + SM_Q, 16, 1024);        // q, K-major (scores)
+      const uint64_t ddo0 = sdesc_sw128(sb + SM_DO, 16, 1024);      // dO, K-major (dP)
+      const uint64_t dk0 = sdesc_sw128(sb + SM_KV, 16, 1024);       // K rows, K-major (scores, dP)
+      const uint64_t dkt0 = sdesc_sw128(sb + SM_KV, kChunkKV, 1024); // K rows read MN-major (dQ)
+      const uint64_t dqt0 = sdesc_sw128(sb + SM_Q, kChunk, 1024);   // q^T, MN-major (dKV)
+      const uint64_t ddot0 = sdesc_sw128(sb + SM_DO, kChunk, 1024); // dO^T, MN-major (dKV)
+      const uint64_t dsa0 = sdesc_sw64(sb + SM_DS, 16, 512);        // dS' as the K-major A of dQ
+      const uint64_t dpb0 = sdesc_sw64(sb + SM_P, 8192, 512);       // P / dS' rows as MN-major B of dKV
+      static_assert(SM_P <= SM_DS && SM_P <= SM_DSLO && SM_P <= SM_PLO, "offsets from SM_P are non-negative");
       bool ok = mbar_wait(bar_addr(sb, QD_FULL), 0, abort_flag, p.status);
       // iteration i issues S/dP of block i, then dQ/dKV of block i-1, so the
       // score MMAs of the next block run while the softmax warps work
       for (int i = 0; ok && i <= nblk; ++i) {
         if (i < nblk) {
           const int st = i & 1;
-          const uint32_t kvb = sb + SM_KV + st * kStage;
           if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
           if (i >= 1 && !(ok = mbar_wait(bar_addr(sb, SDP_FREE), (i - 1) & 1, abort_flag, p.status))) break;
           fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
           // S_half = q_half K_half^T ; dP_half = dO_half V_half^T   (K-major operands, 128B swizzle)
-          for (int k = 0; k < nch; ++k)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_bf16_ss(tmem + TM_S, sdesc_sw128(sb + SM_Q + k * kChunk + ks * 32, 16, 1024),
-                          sdesc_sw128(kvb + k * kChunkKV + ks * 32, 16, 1024), id_sdp, (k | ks) != 0);
+          for (int k = 0; k < 5; ++k) {
+            if (k < nch) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + TM_S, sdesc_add(dq0, k * kChunk + ks * 32),
+                            sdesc_add(dk0, st * kStage + k * kChunkKV + ks * 32), id_sdp, (k | ks) != 0);
+            }
+          }
+#pragma unroll
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              mma_bf16_ss(tmem + TM_DP, sdesc_sw128(sb + SM_DO + k * kChunk + ks * 32, 16, 1024),
-                          sdesc_sw128(kvb + k * kChunkKV + ks * 32, 16, 1024), id_sdp, (k | ks) != 0);
+              mma_bf16_ss(tmem + TM_DP, sdesc_add(ddo0, k * kChunk + ks * 32),
+                          sdesc_add(dk0, st * kStage + k * kChunkKV + ks * 32), id_sdp, (k | ks) != 0);
           mma_commit(bar_addr(sb, SDP_FULL));
         }
         if (i >= 1) {
           const int j = i - 1, stj = j & 1;
-          const uint32_t kvb = sb + SM_KV + stj * kStage;
           if (!(ok = mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status))) break;
           tc_fence_after();
           // dQ_half += (hi + lo) K_half: A = dS' (K-major, 64B swizzle), B = K block read MN-major
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
-            const uint32_t dsb = part == 0 ? SM_DS : SM_DSLO;
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-              const uint64_t ad = sdesc_sw64(sb + dsb + ks * 32, 16, 512);
+              const uint64_t ad = sdesc_add(dsa0, (part == 0 ? 0 : SM_DSLO - SM_DS) + ks * 32);
               const uint32_t acc = (j > 0 || part > 0 || ks > 0);
-              mma_bf16_ss(tmem + TM_DQ, ad, sdesc_sw128(kvb + ks * 16 * 128, kChunkKV, 1024), id_dq256, acc);
-              if (nch == 5)
-                mma_bf16_ss(tmem + TM_DQ + 256, ad,
-                            sdesc_sw128(kvb + 4 * kChunkKV + ks * 16 * 128, kChunkKV, 1024), id_dq64, acc);
+              const uint32_t koff = stj * kStage + ks * 16 * 128;
+              mma_bf16_ss(tmem + TM_DQ, ad, sdesc_add(dkt0, koff), id_dq256, acc);
+              if (nch == 5) mma_bf16_ss(tmem + TM_DQ + 256, ad, sdesc_add(dkt0, koff + 4 * kChunkKV), id_dq64, acc);
             }
           }
           // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
@@ -249,17 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             const uint32_t d_t = tmem + TM_DKV + 32 * m;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = sdesc_sw128(sb + SM_Q + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024);
-              mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_DS + ks * 16 * 64, 8192, 512), id_dkv, ks != 0);
-              mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_DSLO + ks * 16 * 64, 8192, 512), id_dkv, 1);
+              const uint64_t ad = sdesc_add(dqt0, 2 * m * kChunk + ks * 16 * 128);
+              mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_DS - SM_P + ks * 16 * 64), id_dkv, ks != 0);
+              mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_DSLO - SM_P + ks * 16 * 64), id_dkv, 1);
             }
             if (2 * m < 4) {   // tiles inside the value range also get the dO^T P term
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
               {
-                const uint64_t ad = sdesc_sw128(sb + SM_DO + 2 * m * kChunk + ks * 16 * 128, kChunk, 1024);
-                mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_P + ks * 16 * 64, 8192, 512), id_dkv, 1);
-                mma_bf16_ss(d_t, ad, sdesc_sw64(sb + SM_PLO + ks * 16 * 64, 8192, 512), id_dkv, 1);
+                const uint64_t ad = sdesc_add(ddot0, 2 * m * kChunk + ks * 16 * 128);
+                mma_bf16_ss(d_t, ad, sdesc_add(dpb0, ks * 16 * 64), id_dkv, 1);
+                mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_PLO - SM_P + ks * 16 * 64), id_dkv, 1);
               }
             }
           }

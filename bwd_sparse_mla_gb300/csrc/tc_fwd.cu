@@ -181,6 +181,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
       const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      // base descriptors; per-MMA descriptors only move the start address
+      const uint64_t dq0 = sdesc_sw128(sb + SM_Q, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sb + SM_KV, 16, 1024);
+      const uint64_t dp0 = sdesc_sw128(sb + SM_P, 16, 1024);
+      // V is the first four chunks of the stage, read MN-major:
+      // LBO = stride between 64-dim chunks, SBO = stride between 8-row groups
+      const uint64_t dv0 = sdesc_sw128(sb + SM_KV, kChunkKV, 1024);
       bool ok = mbar_wait(bar_addr(sb, Q_FULL), 0, abort_flag, p.status);
       for (int i = 0; ok && i <= nblk; ++i) {
         if (i < nblk) {
@@ -189,12 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           if (i >= 2 && !mbar_wait(bar_addr(sb, S_FREE + b), ((i - 2) >> 1) & 1, abort_flag, p.status)) break;
           fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
-          for (int k = 0; k < nch; ++k) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = sdesc_sw128(sb + SM_Q + k * kChunkQ + ks * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sb + SM_KV + st * kStageBytes + k * kChunkKV + ks * 32, 16, 1024);
-              mma_bf16_ss(tmem + TM_S + 64 * b, ad, bd, idesc_s, (k | ks) != 0);
+          for (int k = 0; k < 5; ++k) {
+            if (k < nch) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + TM_S + 64 * b, sdesc_add(dq0, k * kChunkQ + ks * 32),
+                            sdesc_add(dk0, st * kStageBytes + k * kChunkKV + ks * 32), idesc_s, (k | ks) != 0);
             }
           }
           mma_commit(bar_addr(sb, S_FULL + b));
@@ -204,13 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           if (!mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status)) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = sdesc_sw128(sb + SM_P + ks * 32, 16, 1024);
-            // V is the first four chunks of the stage, read MN-major:
-            // LBO = stride between 64-dim chunks, SBO = stride between 8-row groups
-            const uint64_t bd = sdesc_sw128(sb + SM_KV + stj * kStageBytes + ks * 16 * 128, kChunkKV, 1024);
-            mma_bf16_ss(tmem + TM_O, ad, bd, idesc_pv, (j > 0 || ks > 0));
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tmem + TM_O, sdesc_add(dp0, ks * 32), sdesc_add(dv0, stj * kStageBytes + ks * 16 * 128),
+                        idesc_pv, (j > 0 || ks > 0));
           mma_commit(bar_addr(sb, O_DONE));
           mma_commit(bar_addr(sb, KV_EMPTY + stj));
         }
