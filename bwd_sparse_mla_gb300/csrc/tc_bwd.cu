@@ -46,26 +46,25 @@ constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4
 constexpr int kChunk = 128 * 128;       // 64-dim chunk of q / dO for 128 heads
 constexpr int kChunkKV = kBK * 128;     // 64-dim chunk of a 32-row KV block
 constexpr int kStage = 5 * kChunkKV;
-constexpr int kXPitch = 272;
 
 constexpr int SM_Q = 0;                                 // 5 chunks
 constexpr int SM_DO = SM_Q + 5 * kChunk;                // 4 chunks
 constexpr int SM_KV = SM_DO + 4 * kChunk;               // 2 stages
-constexpr int SM_X = SM_KV + 2 * kStage;                // exchange rows, then P / dS
-constexpr int SM_P = SM_X;                              // 128 rows x 64 B, 64B swizzle
-constexpr int SM_DS = SM_X + 128 * 64;                 // dS' hi
-constexpr int SM_DSLO = SM_X + 2 * 128 * 64;            // dS' lo
-constexpr int SM_PLO = SM_X + 3 * 128 * 64;             // P lo
-constexpr int SM_ROWS = SM_X + 128 * kXPitch;           // 2 x 32 int32
+constexpr int SM_P = SM_KV + 2 * kStage;               // 128 rows x 64 B, 64B swizzle
+constexpr int SM_DS = SM_P + 128 * 64;                  // dS' hi
+constexpr int SM_DSLO = SM_P + 2 * 128 * 64;            // dS' lo
+constexpr int SM_PLO = SM_P + 3 * 128 * 64;             // P lo
+constexpr int SM_ROWS = SM_P + 4 * 128 * 64;            // 2 x 32 int32
 constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
 constexpr int SM_BAR = SM_MASK + 8;
-enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 8,
-           P_FULL = 9, PDS_FREE = 10, DKV_FULL = 11, DKV_FREE = 12, X_READ = 13, NBAR = 14 };
+enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 9,
+           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, NBAR = 15 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
-constexpr int SM_ABORT = SM_TMEM + 4;
+constexpr int SM_SMID = SM_TMEM + 8;
+constexpr int SM_ABORT = SM_SMID + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;
-static_assert(SM_X % 1024 == 0, "swizzle atoms");
-static_assert(SM_PLO + 128 * 64 <= SM_X + 128 * kXPitch, "P, dS' (hi and lo) and P lo fit in the exchange area");
+static_assert(SM_P % 1024 == 0, "swizzle atoms");
+static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the exchange scratch is indexed by SM");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
@@ -76,6 +75,7 @@ constexpr uint32_t TM_DKV = 384;        // up to 3 tiles x 32
 
 struct TcBwdParams {
   const uint16_t* kv;
+  float* xchg;                          // exchange scratch, kXchgSlots slots
   const int32_t* indices;
   const float* lse;
   const float* delta;
@@ -114,15 +114,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FREE), 128);
-    mbar_init(bar_addr(sb, X_FULL), 1);     // armed with the bytes the peer sends
-    mbar_init(bar_addr(sb, X_EMPTY), 1);    // the peer's exchange area is free and armed
+    mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
+    mbar_init(bar_addr(sb, X_FULL + 1), 128);
+    mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
+    mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
     mbar_init(bar_addr(sb, DKV_FREE), 128);
-    mbar_init(bar_addr(sb, X_READ), 128);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);   // block 0's partials from the peer
+    *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sb + SM_TMEM, kTmemCols);
@@ -286,10 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xrow = sb + SM_X + h * kXPitch;
-    const uint32_t xrow_peer = mapa(xrow, peer);
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    // exchange slots of this CTA's SM and of the peer's SM
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
+    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     const float lse2 = p.lse[(int64_t)t * 128 + h] * kLog2e;
     const float dl = p.delta[(int64_t)t * 128 + h];
     uint8_t* prow = smem + SM_P + h * 64;
@@ -307,38 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_ld32(tl + TM_DP, dp);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, SDP_FREE));
-      if (i >= 1) {
-        // once this CTA's MMAs are done with P / dS' (which live in its exchange
-        // area), re-arm the area and let the peer send the next partial rows
-        int okx = 1;
-        if (h == 0) {
-          okx = mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status);
-          if (okx) {
-            mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);
-            mbar_arrive_remote(xempty_peer);
-          }
-        }
-        if (!(ok = __all_sync(0xffffffffu, okx))) break;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))) break;
-      }
-      // partial rows to the peer: st.async counts the bytes on the peer's X_FULL
-#pragma unroll
-      for (int v = 0; v < 8; ++v)
-        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
-#pragma unroll
-      for (int v = 0; v < 8; ++v)
-        st_async_v4(xrow_peer + 128 + 16 * v, dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3], xfull_peer);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
-      const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
+      // exchange the partial S / dP rows through L2: write ours into buffer
+      // i&1 of this SM's slot, read the peer's from its slot
+      const int xb = i & 1;
+      if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
+                                                                   abort_flag, p.status))))
+        break;
+      float4* wr = xmine + xb * (kXchgBufFloats / 4);
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
-        const float4 a = xr[v], b = xr[8 + v];
-        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
-        dp[4 * v] += b.x; dp[4 * v + 1] += b.y; dp[4 * v + 2] += b.z; dp[4 * v + 3] += b.w;
+        wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+        wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
       }
-      // every exchange row is read before P / dS' overwrite the area
-      mbar_arrive(bar_addr(sb, X_READ));
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, X_READ), i & 1, abort_flag, p.status)))) break;
+      mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
+        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
+      }
+      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
       uint32_t pp[16], dd[16], dl2[16], pl[16];
@@ -353,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         dd[j] = pack_bf16x2(d0, d1);
         dl2[j] = pack_bf16x2(d0 - bf16_lo(dd[j]), d1 - bf16_hi(dd[j]));   // the part bf16 dropped
       }
+      // P / dS' buffers are free once this CTA's dQ / dKV MMAs of the previous block completed
+      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status))))
+        break;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
@@ -458,16 +456,18 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 }  // namespace
 
 uint32_t* tc_status_ptr();
+float* tc_xchg_ptr();
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap tm_q, tm_do;
   if (!make_map(&tm_q, a.q, kDqk, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tm_do, a.dout, kDv, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
   uint32_t* status = tc_status_ptr();
-  if (!status) return cudaErrorInvalidSymbol;
+  float* xchg = tc_xchg_ptr();
+  if (!status || !xchg) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  TcBwdParams p{a.kv, a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
+  TcBwdParams p{a.kv, xchg, a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
   tc_bwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }

@@ -102,6 +102,33 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+// 16-byte global load that bypasses L1 (the data was written by another SM)
+__device__ __forceinline__ float4 ld_cg_v4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Score-exchange scratch in global memory (L2): one slot per SM, two block
+// buffers per slot, each 16 chunks x 128 heads x 16 bytes (32 KiB), chunk-major
+// so that a warp's 16-byte accesses for one chunk are contiguous.  A slot is
+// used only by the CTA running on that SM; the tensor-core kernels need more
+// than half of an SM's shared memory, so no two of their CTAs share an SM.
+constexpr int kXchgSlots = 256;
+constexpr int kXchgBufFloats = 16 * 128 * 4;          // 32 KiB
+constexpr int kXchgSlotFloats = 2 * kXchgBufFloats;   // 64 KiB
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -7,8 +7,8 @@
 // rows, so the pair reads every gathered byte exactly once, and each CTA
 // holds an O accumulator of 128 heads x 256 dims (256 TMEM columns).  The
 // partial scores of the two halves are exchanged through distributed shared
-// memory and summed in both CTAs (a + b == b + a, so both see bit-identical
-// scores and take identical softmax decisions).
+// memory (L2) and summed in both CTAs (a + b == b + a, so both see
+// bit-identical scores and take identical softmax decisions).
 //
 // Per block of 64 top-k slots:
 //   producer warps: read the 64 indices (one block ahead), mask them (valid
@@ -19,12 +19,11 @@
 //                   fix, implementation breakdown item 2);
 //   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
 //                   into TMEM, then O += P V_half (M=128, N=256, K=64);
-//   sender warps  : one thread per head: load the 64 partial scores and send
-//                   them to the peer CTA with st.async (which signals the
-//                   peer's mbarrier as the bytes land), one block ahead of
-//                   the softmax warps, so the exchange overlaps the softmax;
-//   softmax warps : one thread per head: load the 64 partial scores, add the
-//                   peer's partials, mask padding to -inf, online
+//   softmax warps : one thread per head: load the 64 partial scores, write
+//                   them to this SM's slot of an L2 exchange scratch (double
+//                   buffered by block parity), signal the peer CTA through its
+//                   mbarrier, add the peer's partials read from its slot,
+//                   mask padding to -inf, online
 //                   softmax in the exp2 domain with a lazily updated running
 //                   max, rescale O in TMEM when the max moves, write P (bf16)
 //                   for the PV MMA.  At the end the sum of exponentials is
@@ -41,30 +40,29 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax, 7..10 senders
+constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax
 constexpr int kMmaWarp = 2;
-constexpr int kSenderWarp0 = 7;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
-constexpr int kThreads = kProducers + 32 + 128 + 128;
+constexpr int kThreads = kProducers + 32 + 128;
 constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
-constexpr int kXPitch = 272;            // bytes per exchanged score row (64 fp32 + pad)
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int SM_Q = 0;
 constexpr int SM_KV = SM_Q + 5 * kChunkQ;           // 2 stages
 constexpr int SM_P = SM_KV + 2 * kStageBytes;
-constexpr int SM_X = SM_P + 128 * 128;
-constexpr int SM_MASK = SM_X + 128 * kXPitch;       // 2 x u64
+constexpr int SM_MASK = SM_P + 128 * 128;          // 2 x u64
 constexpr int SM_BAR = SM_MASK + 16;
-enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 10,
-           P_FULL = 11, O_DONE = 12, X_READ = 13, NBAR = 14 };
+enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 11,
+           P_FULL = 13, O_DONE = 14, NBAR = 15 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
-constexpr int SM_ABORT = SM_TMEM + 4;
+constexpr int SM_SMID = SM_TMEM + 4;
+constexpr int SM_ABORT = SM_SMID + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the exchange scratch is indexed by SM");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;            // 256 columns
@@ -72,6 +70,7 @@ constexpr uint32_t TM_S = 256;          // 2 x 64 columns
 
 struct TcFwdParams {
   const uint16_t* kv;                   // [T, 576] bf16
+  float* xchg;                          // exchange scratch, kXchgSlots slots
   const int32_t* indices;
   uint16_t* out;
   float* lse;
@@ -105,15 +104,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, Q_FULL), 1);
     mbar_init(bar_addr(sb, S_FULL + 0), 1);
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
-    mbar_init(bar_addr(sb, S_FREE + 0), 256);   // softmax and sender threads have read the scores
-    mbar_init(bar_addr(sb, S_FREE + 1), 256);
-    mbar_init(bar_addr(sb, X_FULL), 1);         // armed here with the bytes the peer sends
-    mbar_init(bar_addr(sb, X_EMPTY), 1);        // the peer has read our partials and re-armed
+    mbar_init(bar_addr(sb, S_FREE + 0), 128);
+    mbar_init(bar_addr(sb, S_FREE + 1), 128);
+    mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
+    mbar_init(bar_addr(sb, X_FULL + 1), 128);
+    mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
+    mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, O_DONE), 1);
-    mbar_init(bar_addr(sb, X_READ), 128);       // all softmax threads have read the peer's partials
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);   // block 0's partial scores from the peer
+    *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sb + SM_TMEM, kTmemCols);
@@ -221,12 +221,18 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
     __syncwarp();
-  } else if (warp < kSenderWarp0) {
+  } else {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int h = 32 * q4 + lane;            // head == TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    // exchange slots of this CTA's SM and of the peer's SM
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
+    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     uint8_t* prow = smem + SM_P + h * 128;
     // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
     // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
@@ -240,24 +246,25 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_ld64(tl + TM_S + 64 * b, s);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_FREE + b));
-      // the peer's partial scores for this block (sent by its sender warps)
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL), i & 1, abort_flag, p.status)))) break;
-      const float4* xr = reinterpret_cast<const float4*>(smem + SM_X + h * kXPitch);
+      // exchange the partial scores through L2: write ours into buffer i&1 of
+      // this SM's slot, read the peer's from its slot
+      const int xb = i & 1;
+      if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
+                                                                   abort_flag, p.status))))
+        break;
+      float4* wr = xmine + xb * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v = 0; v < 16; ++v) wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+      mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
-        const float4 o = xr[v];
+        const float4 o = ld_cg_v4(rd + v * 128);
         s[4 * v] += o.x; s[4 * v + 1] += o.y; s[4 * v + 2] += o.z; s[4 * v + 3] += o.w;
       }
-      mbar_arrive(bar_addr(sb, X_READ));
-      int okx = 1;
-      if (h == 0) {                            // once all rows are read: re-arm, then let the peer send
-        okx = mbar_wait(bar_addr(sb, X_READ), i & 1, abort_flag, p.status);
-        if (okx) {
-          mbar_arrive_expect_tx(bar_addr(sb, X_FULL), 128 * 256);
-          mbar_arrive_remote(xempty_peer);
-        }
-      }
-      if (!(ok = __all_sync(0xffffffffu, okx))) break;
+      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       // slot validity of this block (written by the producer before it armed KV_FULL)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
@@ -326,29 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
       if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
     }
-    } else {
-    // ------------------------------------------------------------ senders
-    const int q4 = warp & 3;
-    const int h = 32 * q4 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xrow_peer = mapa(sb + SM_X + h * kXPitch, peer);
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    for (int i = 0; i < nblk; ++i) {
-      const int b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (i >> 1) & 1, abort_flag, p.status))) break;
-      tc_fence_after();
-      float s[64];
-      tmem_ld64(tl + TM_S + 64 * b, s);
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, S_FREE + b));
-      // the peer has read the previous block's partials and re-armed its X_FULL
-      if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY), (i - 1) & 1, abort_flag, p.status)))
-        break;
-#pragma unroll
-      for (int v = 0; v < 16; ++v)
-        st_async_v4(xrow_peer + 16 * v, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], xfull_peer);
     }
-  }
 
   // ------------------------------------------------------------ teardown
   if (*abort_flag) __nanosleep(1000000);   // let copies and MMAs already issued land
@@ -362,6 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 }
 
 __device__ uint32_t g_status = 0;
+// exchange scratch of the tensor-core kernels (16 MiB), one slot per SM
+__device__ __align__(256) float g_xchg[kXchgSlots * kXchgSlotFloats];
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -401,6 +388,12 @@ uint32_t* tc_status_ptr() {
   return static_cast<uint32_t*>(p);
 }
 
+float* tc_xchg_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_xchg) != cudaSuccess) return nullptr;
+  return static_cast<float*>(p);
+}
+
 cudaError_t read_tc_status(uint32_t* out, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(uint32_t));
   if (e == cudaSuccess && clear) {
@@ -417,7 +410,9 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (!status) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  TcFwdParams p{a.kv, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
+  float* xchg = tc_xchg_ptr();
+  if (!xchg) return cudaErrorInvalidSymbol;
+  TcFwdParams p{a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
   tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, p);
   return cudaGetLastError();
 }
