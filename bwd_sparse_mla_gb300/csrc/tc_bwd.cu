@@ -13,9 +13,11 @@
 //              zero bytes: exact-zero K/V rows);
 //   MMA      : S_half = q_half K_half^T and dP_half = dO_half V_half^T
 //              (M=128 heads, N=32 slots) into TMEM;
-//   softmax  : one thread per head sends its partial S and dP rows to the
-//              peer CTA with st.async, sums them with the peer's partials
-//              (both CTAs obtain bit-identical sums), recomputes
+//   exchange : one thread per head writes its partial S and dP rows to this
+//              SM's slot of an L2 exchange scratch, reads the peer CTA's rows
+//              from its slot, and stores the sums back into TMEM (both CTAs
+//              obtain bit-identical sums);
+//   softmax  : one thread per head loads the full S and dP rows, recomputes
 //              P = exp2(S*scale*log2e - lse*log2e) (0 on padding slots),
 //              dS' = scale * P * (dP - Delta), and stores P and dS' each as
 //              a bf16 pair hi + lo (x - hi rounded again), so the dQ and dKV
@@ -23,7 +25,7 @@
 //   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
 //              transposed dKV tiles dKV^T[d, j] = dO^T (hi + lo) + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
-//   drain    : four warps read the dKV tiles from TMEM and add them into the
+//   drain    : the exchange warps also read the dKV tiles from TMEM and add them into the
 //              fp32 dKV rows named by the valid slots (coalesced 128-byte
 //              fp32 reductions; padding slots issue no write, the no-op the
 //              miles PR #2079 summary describes for the clamped atomic).
@@ -38,7 +40,7 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 32;
-constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax, w7..10 dKV drain
+constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax, w7..10 exchange + dKV drain
 constexpr int kMmaWarp = 2;
 constexpr int kDrainWarp0 = 7;
 constexpr int kThreads = 352;
@@ -55,10 +57,11 @@ constexpr int SM_DS = SM_P + 128 * 64;                  // dS' hi
 constexpr int SM_DSLO = SM_P + 2 * 128 * 64;            // dS' lo
 constexpr int SM_PLO = SM_P + 3 * 128 * 64;             // P lo
 constexpr int SM_ROWS = SM_P + 4 * 128 * 64;            // 2 x 32 int32
-constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
+constexpr int SM_DROWS = SM_ROWS + 2 * 32 * 4;          // drain warps' copies of the row list, 4 x 2 x 32 int32
+constexpr int SM_MASK = SM_DROWS + 4 * 2 * 32 * 4;      // 2 x u32
 constexpr int SM_BAR = SM_MASK + 8;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 9,
-           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, NBAR = 15 };
+           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, S_SUM = 15, NBAR = 16 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 8;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -122,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
     mbar_init(bar_addr(sb, DKV_FREE), 128);
+    mbar_init(bar_addr(sb, S_SUM), 128);        // full S / dP stored back into TMEM
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -287,13 +291,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
-    // exchange slots of this CTA's SM and of the peer's SM
-    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
-    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
-    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     const float lse2 = p.lse[(int64_t)t * 128 + h] * kLog2e;
     const float dl = p.delta[(int64_t)t * 128 + h];
     uint8_t* prow = smem + SM_P + h * 64;
@@ -304,36 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int st = i & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM), i & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[32], dp[32];
-      tmem_ld32(tl + TM_S, s);
+      tmem_ld32(tl + TM_S, s);          // full rows (own + peer partials)
       tmem_ld32(tl + TM_DP, dp);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, SDP_FREE));
-      // exchange the partial S / dP rows through L2: write ours into buffer
-      // i&1 of this SM's slot, read the peer's from its slot
-      const int xb = i & 1;
-      if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
-                                                                   abort_flag, p.status))))
-        break;
-      float4* wr = xmine + xb * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-        wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
-      }
-      mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
-        break;
-      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
-        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
-        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
-      }
-      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
       uint32_t pp[16], dd[16], dl2[16], pl[16];
@@ -380,37 +354,88 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ dKV drain
+    // ------------------------------------------------------------ exchange + dKV drain
     const int q4 = warp & 3;
-    const int L = 32 * q4 + lane;               // TMEM lane = dim within a 128-dim tile
+    const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
     const int dbase = 256 * (int)crank;          // first key dim of this CTA
-    for (int i = 0; i < nblk; ++i) {
-      const int st = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), i & 1, abort_flag, p.status))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
-      int rows[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) rows[j] = srows[st * 32 + j];
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
+    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + L;
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + L;
+
+    // drain block j's dKV tiles into the fp32 rows its valid slots name
+    auto drain = [&](int j) -> bool {
+      const int st = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, p.status))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (j >> 1) & 1, abort_flag, p.status))) return false;
+      // keep a per-warp copy of the block's rows, so the stage can be refilled
+      int* drows = reinterpret_cast<int*>(smem + SM_DROWS) + ((warp - kDrainWarp0) * 2 + (j & 1)) * 32;
+      drows[lane] = srows[st * 32 + lane];
+      __syncwarp();
       mbar_arrive(bar_addr(sb, KV_EMPTY + st));
       tc_fence_after();
-      float g[3][32];
-#pragma unroll
-      for (int m = 0; m < 3; ++m)
-        if (m < ntile) tmem_ld32(tl + TM_DKV + 32 * m, g[m]);
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, DKV_FREE));
-#pragma unroll
-      for (int m = 0; m < 3; ++m) {
+#pragma unroll 1
+      for (int m = 0; m < ntile; ++m) {
+        float g[32];
+        tmem_ld32(tl + TM_DKV + 32 * m, g);
+        if (m == ntile - 1) {               // every tile is in registers: the MMA may overwrite them
+          tc_fence_before();
+          mbar_arrive(bar_addr(sb, DKV_FREE));
+        }
         const int d = dbase + 128 * m + L;
-        if (m < ntile && d < kDqk) {
+        if (d < kDqk) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (rows[j] >= 0) red_add_f32(p.dkv32 + (int64_t)rows[j] * kDqk + d, g[m][j]);
+          for (int k = 0; k < 32; ++k) {
+            const int row = drows[k];
+            if (row >= 0) red_add_f32(p.dkv32 + (int64_t)row * kDqk + d, g[k]);
+          }
         }
       }
+      return true;
+    };
+
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      // exchange block i: partial S / dP rows through L2, buffer i&1 of the SM slots
+      const int xb = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
+      tc_fence_after();
+      float s[32], dp[32];
+      tmem_ld32(tl + TM_S, s);
+      tmem_ld32(tl + TM_DP, dp);
+      if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
+                                                                   abort_flag, p.status))))
+        break;
+      float4* wr = xmine + xb * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+        wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
+      }
+      mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
+        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
+      }
+      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
+      tmem_st32(tl + TM_S, s);
+      tmem_st32(tl + TM_DP, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, S_SUM));
+      // then drain the previous block's dKV tiles
+      if (i >= 1 && !(ok = drain(i - 1))) break;
     }
+    if (ok && nblk > 0) drain(nblk - 1);
   }
 
   // ------------------------------------------------------------ teardown

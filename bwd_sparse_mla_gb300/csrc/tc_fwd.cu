@@ -19,11 +19,14 @@
 //                   fix, implementation breakdown item 2);
 //   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
 //                   into TMEM, then O += P V_half (M=128, N=256, K=64);
-//   softmax warps : one thread per head: load the 64 partial scores, write
+//   exchange warps: one thread per head: load the 64 partial scores, write
 //                   them to this SM's slot of an L2 exchange scratch (double
 //                   buffered by block parity), signal the peer CTA through its
-//                   mbarrier, add the peer's partials read from its slot,
-//                   mask padding to -inf, online
+//                   mbarrier, add the peer's partials read from its slot and
+//                   store the full scores back into TMEM; software pipelined
+//                   one block ahead, so the exchange latency overlaps;
+//   softmax warps : one thread per head: load the full scores, mask padding
+//                   to -inf, online
 //                   softmax in the exp2 domain with a lazily updated running
 //                   max, rescale O in TMEM when the max moves, write P (bf16)
 //                   for the PV MMA.  At the end the sum of exponentials is
@@ -40,10 +43,11 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax
+constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax, 7..10 exchange
 constexpr int kMmaWarp = 2;
+constexpr int kXchgWarp0 = 7;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
-constexpr int kThreads = kProducers + 32 + 128;
+constexpr int kThreads = kProducers + 32 + 128 + 128;
 constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
@@ -56,7 +60,7 @@ constexpr int SM_P = SM_KV + 2 * kStageBytes;
 constexpr int SM_MASK = SM_P + 128 * 128;          // 2 x u64
 constexpr int SM_BAR = SM_MASK + 16;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 11,
-           P_FULL = 13, O_DONE = 14, NBAR = 15 };
+           P_FULL = 13, O_DONE = 14, S_SUM = 15, NBAR = 17 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 4;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -104,8 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, Q_FULL), 1);
     mbar_init(bar_addr(sb, S_FULL + 0), 1);
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
-    mbar_init(bar_addr(sb, S_FREE + 0), 128);
+    mbar_init(bar_addr(sb, S_FREE + 0), 128);   // softmax threads loaded the full scores
     mbar_init(bar_addr(sb, S_FREE + 1), 128);
+    mbar_init(bar_addr(sb, S_SUM + 0), 128);    // exchange threads stored the full scores
+    mbar_init(bar_addr(sb, S_SUM + 1), 128);
     mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
     mbar_init(bar_addr(sb, X_FULL + 1), 128);
     mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
@@ -221,18 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kXchgWarp0) {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int h = 32 * q4 + lane;            // head == TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
-    // exchange slots of this CTA's SM and of the peer's SM
-    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
-    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
-    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     uint8_t* prow = smem + SM_P + h * 128;
     // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
     // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
@@ -240,31 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int b = i & 1, st = i & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (i >> 1) & 1, abort_flag, p.status)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM + b), (i >> 1) & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[64];
-      tmem_ld64(tl + TM_S + 64 * b, s);
+      tmem_ld64(tl + TM_S + 64 * b, s);     // full scores (own + peer partials)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_FREE + b));
-      // exchange the partial scores through L2: write ours into buffer i&1 of
-      // this SM's slot, read the peer's from its slot
-      const int xb = i & 1;
-      if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
-                                                                   abort_flag, p.status))))
-        break;
-      float4* wr = xmine + xb * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v = 0; v < 16; ++v) wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-      mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
-        break;
-      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v = 0; v < 16; ++v) {
-        const float4 o = ld_cg_v4(rd + v * 128);
-        s[4 * v] += o.x; s[4 * v + 1] += o.y; s[4 * v + 2] += o.z; s[4 * v + 3] += o.w;
-      }
-      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       // slot validity of this block (written by the producer before it armed KV_FULL)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
@@ -333,7 +313,55 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
       if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
     }
+      } else {
+    // ------------------------------------------------------------ exchange
+    const int q4 = warp & 3;
+    const int h = 32 * q4 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    // exchange slots of this CTA's SM and of the peer's SM
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
+    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
+    float cur[64], nxt[64];
+    // load block j's partial scores and publish them to the peer
+    auto publish = [&](int j, float* v) -> bool {
+      const int b = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (j >> 1) & 1, abort_flag, p.status))) return false;
+      tc_fence_after();
+      tmem_ld64(tl + TM_S + 64 * b, v);
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + b), ((j >> 1) - 1) & 1, abort_flag,
+                                                              p.status)))
+        return false;
+      float4* wr = xmine + b * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+      mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
+      return true;
+    };
+    bool ok = nblk > 0 && publish(0, cur);
+    for (int i = 0; ok && i < nblk; ++i) {
+      const int b = i & 1;
+      if (i + 1 < nblk && !(ok = publish(i + 1, nxt))) break;   // one block ahead
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), (i >> 1) & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + b * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v4 = 0; v4 < 16; ++v4) {
+        const float4 o = ld_cg_v4(rd + v4 * 128);
+        cur[4 * v4] += o.x; cur[4 * v4 + 1] += o.y; cur[4 * v4 + 2] += o.z; cur[4 * v4 + 3] += o.w;
+      }
+      mbar_arrive_remote(xempty_peer + 8 * b);    // the peer may reuse that buffer
+      tmem_st64(tl + TM_S + 64 * b, cur);         // full scores for the softmax warps
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, S_SUM + b));
+#pragma unroll
+      for (int j = 0; j < 64; ++j) cur[j] = nxt[j];
     }
+  }
 
   // ------------------------------------------------------------ teardown
   if (*abort_flag) __nanosleep(1000000);   // let copies and MMAs already issued land
