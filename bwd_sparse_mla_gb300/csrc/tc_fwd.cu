@@ -23,8 +23,8 @@
 //                   them to this SM's slot of an L2 exchange scratch (double
 //                   buffered by block parity), signal the peer CTA through its
 //                   mbarrier, add the peer's partials read from its slot and
-//                   store the full scores back into TMEM; software pipelined
-//                   one block ahead, so the exchange latency overlaps;
+//                   store the full scores back into TMEM, while the softmax
+//                   warps work on the previous block;
 //   softmax warps : one thread per head: load the full scores, mask padding
 //                   to -inf, online
 //                   softmax in the exp2 domain with a lazily updated running
@@ -55,12 +55,13 @@ constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescale
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int SM_Q = 0;
-constexpr int SM_KV = SM_Q + 5 * kChunkQ;           // 2 stages
-constexpr int SM_P = SM_KV + 2 * kStageBytes;
-constexpr int SM_MASK = SM_P + 128 * 128;          // 2 x u64
-constexpr int SM_BAR = SM_MASK + 16;
-enum Bar { KV_FULL = 0, KV_EMPTY = 2, Q_FULL = 4, S_FULL = 5, S_FREE = 7, X_FULL = 9, X_EMPTY = 11,
-           P_FULL = 13, O_DONE = 14, S_SUM = 15, NBAR = 17 };
+constexpr int kStages = 3;
+constexpr int SM_KV = SM_Q + 5 * kChunkQ;           // kStages stages
+constexpr int SM_P = SM_KV + kStages * kStageBytes;
+constexpr int SM_MASK = SM_P + 128 * 128;          // kStages x u64
+constexpr int SM_BAR = SM_MASK + 8 * kStages;
+enum Bar { KV_FULL = 0, KV_EMPTY = kStages, Q_FULL = 2 * kStages, S_FULL, S_FREE = S_FULL + 2, X_FULL = S_FREE + 2,
+           X_EMPTY = X_FULL + 2, P_FULL = X_EMPTY + 2, O_DONE, S_SUM, NBAR = S_SUM + 2 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 4;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -101,10 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + the slot mask
-    mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
-    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1);
-    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1);
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(bar_addr(sb, KV_FULL + k), kProducers + 1);   // cp.async arrivals + the slot mask
+      mbar_init(bar_addr(sb, KV_EMPTY + k), 1);
+    }
     mbar_init(bar_addr(sb, Q_FULL), 1);
     mbar_init(bar_addr(sb, S_FULL + 0), 1);
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + r0 + RS * j);
     if (warp == 0) { nm[0] = __ldg(irow + lane); nm[1] = __ldg(irow + 32 + lane); }
     for (int i = 0; i < nblk; ++i) {
-      const int st = i & 1;
+      const int st = i % kStages, use = i / kStages;
       int cur[kRowsPerProducer], cm[2];
 #pragma unroll
       for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
@@ -160,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + (i + 1) * kBK + r0 + RS * j);
         if (warp == 0) { nm[0] = __ldg(irow + (i + 1) * kBK + lane); nm[1] = __ldg(irow + (i + 1) * kBK + 32 + lane); }
       }
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag,
-                                                       p.status)))
+      if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), (use - 1) & 1, abort_flag,
+                                                        p.status)))
         break;                                 // warp-uniform exit
       const uint32_t stage = sb + SM_KV + st * kStageBytes;
 #pragma unroll
@@ -197,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       bool ok = mbar_wait(bar_addr(sb, Q_FULL), 0, abort_flag, p.status);
       for (int i = 0; ok && i <= nblk; ++i) {
         if (i < nblk) {
-          const int st = i & 1, b = i & 1;
-          if (!mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)) break;
+          const int st = i % kStages, b = i & 1;
+          if (!mbar_wait(bar_addr(sb, KV_FULL + st), (i / kStages) & 1, abort_flag, p.status)) break;
           if (i >= 2 && !mbar_wait(bar_addr(sb, S_FREE + b), ((i - 2) >> 1) & 1, abort_flag, p.status)) break;
           fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           mma_commit(bar_addr(sb, S_FULL + b));
         }
         if (i >= 1) {
-          const int j = i - 1, stj = j & 1;
+          const int j = i - 1, stj = j % kStages;
           if (!mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status)) break;
           tc_fence_after();
 #pragma unroll
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
-      const int b = i & 1, st = i & 1;
+      const int b = i & 1, st = i % kStages;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM + b), (i >> 1) & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[64];
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_FREE + b));
       // slot validity of this block (written by the producer before it armed KV_FULL)
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i / kStages) & 1, abort_flag, p.status)))) break;
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
       float mx = -INFINITY;
 #pragma unroll
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
     float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
     const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    float cur[64], nxt[64];
+    float cur[64];
     // load block j's partial scores and publish them to the peer
     auto publish = [&](int j, float* v) -> bool {
       const int b = j & 1;
@@ -341,10 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
       return true;
     };
-    bool ok = nblk > 0 && publish(0, cur);
+    bool ok = true;
     for (int i = 0; ok && i < nblk; ++i) {
       const int b = i & 1;
-      if (i + 1 < nblk && !(ok = publish(i + 1, nxt))) break;   // one block ahead
+      if (!(ok = publish(i, cur))) break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), (i >> 1) & 1, abort_flag, p.status))))
         break;
       const float4* rd = xpeer + b * (kXchgBufFloats / 4);
@@ -358,8 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_SUM + b));
-#pragma unroll
-      for (int j = 0; j < 64; ++j) cur[j] = nxt[j];
     }
   }
 
