@@ -52,11 +52,12 @@ constexpr int kStage = 5 * kChunkKV;
 constexpr int SM_Q = 0;                                 // 5 chunks
 constexpr int SM_DO = SM_Q + 5 * kChunk;                // 4 chunks
 constexpr int SM_KV = SM_DO + 4 * kChunk;               // 2 stages
-constexpr int SM_P = SM_KV + 2 * kStage;               // 128 rows x 64 B, 64B swizzle
-constexpr int SM_DS = SM_P + 128 * 64;                  // dS' hi
-constexpr int SM_DSLO = SM_P + 2 * 128 * 64;            // dS' lo
-constexpr int SM_PLO = SM_P + 3 * 128 * 64;             // P lo
-constexpr int SM_ROWS = SM_P + 4 * 128 * 64;            // 2 x 32 int32
+// P and dS' of a block, each as 128 head rows of [hi (32 slots) | lo (32 slots)]
+// bf16 = 128 bytes, 128B swizzle: K-major A of dQ (one half), MN-major B (N = 64)
+// of the dKV products (both halves at once)
+constexpr int SM_P = SM_KV + 2 * kStage;
+constexpr int SM_DS = SM_P + 128 * 128;
+constexpr int SM_ROWS = SM_DS + 128 * 128;              // 2 x 32 int32
 constexpr int SM_DROWS = SM_ROWS + 2 * 32 * 4;          // drain warps' copies of the row list, 4 x 2 x 32 int32
 constexpr int SM_MASK = SM_DROWS + 4 * 2 * 32 * 4;      // 2 x u32
 constexpr int SM_BAR = SM_MASK + 8;
@@ -66,15 +67,14 @@ constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 8;
 constexpr int SM_ABORT = SM_SMID + 4;
 constexpr int kSmemBytes = SM_ABORT + 4 + 1024;
-static_assert(SM_P % 1024 == 0, "swizzle atoms");
+static_assert(SM_P % 1024 == 0 && SM_DS % 1024 == 0, "swizzle atoms");
 static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the exchange scratch is indexed by SM");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_DQ = 0;           // up to 320 columns
-constexpr uint32_t TM_S = 320;          // 32
-constexpr uint32_t TM_DP = 352;         // 32
-constexpr uint32_t TM_DKV = 384;        // up to 3 tiles x 32
+// TMEM columns: dQ [0, ndq), S [ndq, +32), dP [ndq+32, +32), then the dKV^T
+// tiles (64 columns each: hi half | lo half); 256+64+3*64 = 320+64+2*64 = 512
+constexpr uint32_t TM_DQ = 0;
 
 struct TcBwdParams {
   const uint16_t* kv;
@@ -103,8 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   const int t = blockIdx.x >> 1;
   const int nch = 4 + (int)crank;          // key chunks (64 dims each) of this CTA
   const int g0 = 4 * (int)crank;           // first global key chunk; value chunks are g0 .. g0+3
-  const int ntile = 2 + (int)crank;        // 128-dim dKV tiles
+  // q chunks held: the key chunks, and for CTA 0 also the rope tail (chunk 8) in slot 4,
+  // because CTA 0 computes the tail's dKV tile (this balances TMEM between the two)
+  const int ntile = 3 - (int)crank;        // 128-dim dKV tiles: CTA 0 [0,256) + tail, CTA 1 [256,512)
   const int ndq = 64 * nch;                // dQ columns
+  const uint32_t TM_S = ndq, TM_DP = ndq + 32, TM_DKV = ndq + 64;
   const int nblk = p.topk / kBK;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
 
@@ -145,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     if (pt == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (nch + 4) * kChunk);
-      for (int k = 0; k < nch; ++k)
-        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
+      mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (5 + 4) * kChunk);
+      for (int k = 0; k < 5; ++k)
+        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (k < nch ? g0 + k : 8), t * 128, bar_addr(sb, QD_FULL));
       for (int k = 0; k < 4; ++k)
         tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
     }
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const uint32_t id_sdp = idesc_bf16(128, kBK, false, false);
       const uint32_t id_dq256 = idesc_bf16(128, 256, false, true);
       const uint32_t id_dq64 = idesc_bf16(128, 64, false, true);
-      const uint32_t id_dkv = idesc_bf16(128, kBK, true, true);
+      const uint32_t id_dkv = idesc_bf16(128, 2 * kBK, true, true);   // N = 64: hi | lo
       // base descriptors; per-MMA descriptors only move the start address
       const uint64_t dq0 = sdesc_sw128(sb + SM_Q, 16, 1024);        // q, K-major (scores)
       const uint64_t ddo0 = sdesc_sw128(sb + SM_DO, 16, 1024);      // dO, K-major (dP)
@@ -210,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const uint64_t dkt0 = sdesc_sw128(sb + SM_KV, kChunkKV, 1024); // K rows read MN-major (dQ)
       const uint64_t dqt0 = sdesc_sw128(sb + SM_Q, kChunk, 1024);   // q^T, MN-major (dKV)
       const uint64_t ddot0 = sdesc_sw128(sb + SM_DO, kChunk, 1024); // dO^T, MN-major (dKV)
-      const uint64_t dsa0 = sdesc_sw64(sb + SM_DS, 16, 512);        // dS' as the K-major A of dQ
-      const uint64_t dpb0 = sdesc_sw64(sb + SM_P, 8192, 512);       // P / dS' rows as MN-major B of dKV
-      static_assert(SM_P <= SM_DS && SM_P <= SM_DSLO && SM_P <= SM_PLO, "offsets from SM_P are non-negative");
+      const uint64_t dsa0 = sdesc_sw128(sb + SM_DS, 16, 1024);      // dS' halves as the K-major A of dQ
+      const uint64_t dpb0 = sdesc_sw128(sb + SM_P, 8192, 1024);     // P / dS' rows as MN-major B of dKV
+      static_assert(SM_P < SM_DS, "offsets from SM_P are non-negative");
       bool ok = mbar_wait(bar_addr(sb, QD_FULL), 0, abort_flag, p.status);
       // iteration i issues S/dP of block i, then dQ/dKV of block i-1, so the
       // score MMAs of the next block run while the softmax warps work
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-              const uint64_t ad = sdesc_add(dsa0, (part == 0 ? 0 : SM_DSLO - SM_DS) + ks * 32);
+              const uint64_t ad = sdesc_add(dsa0, part * 64 + ks * 32);
               const uint32_t acc = (j > 0 || part > 0 || ks > 0);
               const uint32_t koff = stj * kStage + ks * 16 * 128;
               mma_bf16_ss(tmem + TM_DQ, ad, sdesc_add(dkt0, koff), id_dq256, acc);
@@ -262,21 +265,18 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE), (j - 1) & 1, abort_flag, p.status))) break;
           tc_fence_after();
           for (int m = 0; m < ntile; ++m) {
-            const uint32_t d_t = tmem + TM_DKV + 32 * m;
+            const uint32_t d_t = tmem + TM_DKV + 64 * m;
+            // q^T for this tile: q slots 2m, 2m+1 (CTA 0's tile 2 is the rope tail in slot 4;
+            // its second half reads the next buffer and only lands in TMEM lanes that are not drained)
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = sdesc_add(dqt0, 2 * m * kChunk + ks * 16 * 128);
-              mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_DS - SM_P + ks * 16 * 64), id_dkv, ks != 0);
-              mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_DSLO - SM_P + ks * 16 * 64), id_dkv, 1);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+              mma_bf16_ss(d_t, sdesc_add(dqt0, 2 * m * kChunk + ks * 16 * 128),
+                          sdesc_add(dpb0, SM_DS - SM_P + ks * 16 * 128), id_dkv, ks != 0);
             if (2 * m < 4) {   // tiles inside the value range also get the dO^T P term
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks)
-              {
-                const uint64_t ad = sdesc_add(ddot0, 2 * m * kChunk + ks * 16 * 128);
-                mma_bf16_ss(d_t, ad, sdesc_add(dpb0, ks * 16 * 64), id_dkv, 1);
-                mma_bf16_ss(d_t, ad, sdesc_add(dpb0, SM_PLO - SM_P + ks * 16 * 64), id_dkv, 1);
-              }
+                mma_bf16_ss(d_t, sdesc_add(ddot0, 2 * m * kChunk + ks * 16 * 128), sdesc_add(dpb0, ks * 16 * 128),
+                            id_dkv, 1);
             }
           }
           mma_commit(bar_addr(sb, DKV_FULL));
@@ -293,11 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const float lse2 = p.lse[(int64_t)t * 128 + h] * kLog2e;
     const float dl = p.delta[(int64_t)t * 128 + h];
-    uint8_t* prow = smem + SM_P + h * 64;
-    uint8_t* dsrow = smem + SM_DS + h * 64;
-    uint8_t* dlrow = smem + SM_DSLO + h * 64;
-    uint8_t* plrow = smem + SM_PLO + h * 64;
-    const int sw = (h >> 1) & 3;        // 64B swizzle: 16-byte chunk index ^= address bits [7,9)
+    uint8_t* prow = smem + SM_P + h * 128;
+    uint8_t* dsrow = smem + SM_DS + h * 128;
+    const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
       const int st = i & 1;
@@ -328,10 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
+        *reinterpret_cast<uint4*>(prow + (((c + 4) ^ sw) << 4)) =
+            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
         *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dlrow + ((c ^ sw) << 4)) =
+        *reinterpret_cast<uint4*>(dsrow + (((c + 4) ^ sw) << 4)) =
             make_uint4(dl2[4 * c], dl2[4 * c + 1], dl2[4 * c + 2], dl2[4 * c + 3]);
-        *reinterpret_cast<uint4*>(plrow + ((c ^ sw) << 4)) = make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -359,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
-    const int dbase = 256 * (int)crank;          // first key dim of this CTA
+    // dims of dKV tile m: CTA 0 -> [0,128), [128,256), tail [512,576); CTA 1 -> [256,384), [384,512)
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
     const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
@@ -380,13 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int m = 0; m < ntile; ++m) {
-        float g[32];
-        tmem_ld32(tl + TM_DKV + 32 * m, g);
+        float g[32], glo[32];
+        tmem_ld32(tl + TM_DKV + 64 * m, g);          // hi half
+        tmem_ld32(tl + TM_DKV + 64 * m + 32, glo);   // lo half
         if (m == ntile - 1) {               // every tile is in registers: the MMA may overwrite them
           tc_fence_before();
           mbar_arrive(bar_addr(sb, DKV_FREE));
         }
-        const int d = dbase + 128 * m + L;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) g[k] += glo[k];
+        const int d = (crank == 0 ? (m < 2 ? 128 * m : 512) : 256 + 128 * m) + L;
         if (d < kDqk) {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
