@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_device_status.restype = I
     lib.sparse_mla_launch_count.argtypes = []
     lib.sparse_mla_launch_count.restype = ctypes.c_uint64
+    lib.sparse_mla_wait_selftest.argtypes = [P]
+    lib.sparse_mla_wait_selftest.restype = I
     _lib = lib
     return lib
 
@@ -75,6 +77,13 @@ def sparse_mla_device_status(clear: bool = False) -> int:
     st = ctypes.c_uint32(0)
     _check(load().sparse_mla_device_status(ctypes.byref(st), int(clear)))
     return int(st.value)
+
+
+def sparse_mla_wait_selftest(stream=None) -> None:
+    """Enqueue the bounded-wait self-test: a wait that nothing releases gives
+    up after 1 s and sets the device status word to 1 (read and clear it with
+    sparse_mla_device_status(clear=True))."""
+    _check(load().sparse_mla_wait_selftest(_stream(stream)))
 
 
 def _check(rc: int) -> None:

@@ -91,6 +91,15 @@ int sparse_mla_device_status(uint32_t* status, int clear) {
   return 0;
 }
 
+int sparse_mla_wait_selftest(void* stream) {
+  g_last_error.clear();
+  if (int r = check_device()) return r;
+  cudaError_t e = smla::launch_wait_selftest(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_wait_selftest launch");
+  count_launches(1);
+  return 0;
+}
+
 int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
                    const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
                    smla_bf16_t* out, float* lse, void* stream) {

@@ -79,6 +79,7 @@ cudaError_t launch_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaStr
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t read_tc_status(uint32_t* out, bool clear);
+cudaError_t launch_wait_selftest(cudaStream_t s);
 cudaError_t launch_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
                                  int B, unsigned long long* counter, cudaStream_t s);
 

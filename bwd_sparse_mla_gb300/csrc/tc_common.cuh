@@ -1,5 +1,5 @@
 // Inline-PTX building blocks for the sm_103a tensor-core kernels:
-// mbarriers (with bounded waits), TMA tiled / gather4 loads, thread-block
+// mbarriers (with bounded waits), TMA tiled loads, cp.async gathers, thread-block
 // cluster shared memory, and tcgen05 (TMEM alloc, MMA, commit, ld/st).
 #pragma once
 
@@ -97,10 +97,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ uint32_t smid() {
   uint32_t r;
@@ -141,16 +137,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// Gather four rows (y0..y3) of one box column x into 4 consecutive smem rows.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int x, int y0, int y1, int y2,
-                                            int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
-
 // 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros
 // and reads nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -161,16 +147,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
-// Asynchronous 16-byte store into another CTA's shared memory that signals
-// that CTA's mbarrier (complete_tx of 16 bytes) when it lands.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
-                                            uint32_t cluster_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                   cluster_addr),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -296,17 +272,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 
 // Same descriptor with its start address moved by `bytes` (a multiple of 16).
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
-
-// Shared-memory matrix descriptor with 64-byte swizzle (layout type 4).
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
-}
-
-// Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");

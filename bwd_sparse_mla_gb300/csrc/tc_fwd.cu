@@ -374,6 +374,22 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 }
 
 __device__ uint32_t g_status = 0;
+
+// Failure-detection self-test: one thread waits, through the same bounded
+// wait the tensor-core kernels use, on an mbarrier that nothing arrives on.
+// The wait gives up after its limit, records the timeout in the status word
+// and the kernel returns normally.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status);
+}
 // exchange scratch of the tensor-core kernels (16 MiB), one slot per SM
 __device__ __align__(256) float g_xchg[kXchgSlots * kXchgSlotFloats];
 
@@ -428,6 +444,13 @@ cudaError_t read_tc_status(uint32_t* out, bool clear) {
     e = cudaMemcpyToSymbol(g_status, &z, sizeof(z));
   }
   return e;
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t s) {
+  uint32_t* status = tc_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {

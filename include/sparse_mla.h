@@ -164,6 +164,16 @@ const char* sparse_mla_version(void);
  * word is reset to 0.  Synchronizes with the device. */
 int sparse_mla_device_status(uint32_t* status, int clear);
 
+/* Failure-detection self-test (no counterpart in the source pages).  Enqueues
+ * on `stream` one small kernel whose single thread waits, through the same
+ * bounded wait the tensor-core kernels use, on a barrier that nothing ever
+ * releases.  After the wait limit (1 s) the wait gives up, sets the status
+ * word read by sparse_mla_device_status to 1 and the kernel returns normally:
+ * the CUDA context stays usable.  Callers clear the status word afterwards
+ * (sparse_mla_device_status(&s, 1)); until then it also reports 1 for the
+ * other kernels.  Returns 0, or -EINVAL / -EIO as the other calls. */
+int sparse_mla_wait_selftest(void* stream);
+
 /* Number of CUDA kernels this process has launched through the library so
  * far (all threads, all devices).  Diagnostics only: benchmarks read it
  * before and after a timed region to count the library's launches. */
