@@ -6,9 +6,9 @@
 // CTA 1: [256,512)).  Each CTA gathers only its own columns of the named KV
 // rows, so the pair reads every gathered byte exactly once, and each CTA
 // holds an O accumulator of 128 heads x 256 dims (256 TMEM columns).  The
-// partial scores of the two halves are exchanged through distributed shared
-// memory (L2) and summed in both CTAs (a + b == b + a, so both see
-// bit-identical scores and take identical softmax decisions).
+// partial scores of the two halves are exchanged through an L2 scratch and
+// summed in both CTAs (a + b == b + a, so both see bit-identical scores and
+// take identical softmax decisions).
 //
 // Per block of 64 top-k slots:
 //   producer warps: read the 64 indices (one block ahead), mask them (valid
@@ -18,20 +18,21 @@
 //                   exact-zero K/V row (the clamp + mask of the miles PR #2079
 //                   fix, implementation breakdown item 2);
 //   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
-//                   into TMEM, then O += P V_half (M=128, N=256, K=64);
-//   exchange warps: one thread per head: load the 64 partial scores, write
-//                   them to this SM's slot of an L2 exchange scratch (double
-//                   buffered by block parity), signal the peer CTA through its
-//                   mbarrier, add the peer's partials read from its slot and
-//                   store the full scores back into TMEM, while the softmax
-//                   warps work on the previous block;
-//   softmax warps : one thread per head: load the full scores, mask padding
-//                   to -inf, online
-//                   softmax in the exp2 domain with a lazily updated running
-//                   max, rescale O in TMEM when the max moves, write P (bf16)
-//                   for the PV MMA.  At the end the sum of exponentials is
-//                   floored at 1e-30 (PR #2079 forward fragment), so a row
-//                   with no valid slot gets out = 0 and LSE = ln(1e-30).
+//                   into one of two TMEM score buffers, and O += P V_half
+//                   (M=128, N=256, K=64), each issued as soon as its inputs
+//                   are ready;
+//   two groups of four warps, one thread per head, take alternate blocks:
+//                   load the 64 partial scores, write them to this SM's slot
+//                   of the L2 exchange scratch, signal the peer CTA through
+//                   its mbarrier, add the peer's partials, mask padding to
+//                   -inf and run the online softmax in the exp2 domain with a
+//                   lazily updated running max (handed from group to group
+//                   through shared memory), rescale O in TMEM when the max
+//                   moves, and write P (bf16) for the PV MMA.  One group's
+//                   exchange overlaps the other's softmax.  At the end the sum
+//                   of exponentials is floored at 1e-30 (PR #2079 forward
+//                   fragment), so a row with no valid slot gets out = 0 and
+//                   LSE = ln(1e-30).
 #include <cuda.h>
 
 #include "smla_common.cuh"
@@ -43,25 +44,26 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..6 softmax, 7..10 exchange
+constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..10 two exchange + softmax groups
 constexpr int kMmaWarp = 2;
-constexpr int kXchgWarp0 = 7;
+constexpr int kGroup0 = 3;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
 constexpr int kThreads = kProducers + 32 + 128 + 128;
-constexpr int kChunkQ = 128 * 128;      // one 64-dim chunk of Q: 128 rows x 128 B
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr int SM_Q = 0;
-constexpr int kStages = 3;
-constexpr int SM_KV = SM_Q + 5 * kChunkQ;           // kStages stages
+// shared memory map (offsets from a 1024-aligned base); Q lives in TMEM
+constexpr int kStages = 5;
+constexpr int SM_KV = 0;                           // kStages stages
 constexpr int SM_P = SM_KV + kStages * kStageBytes;
 constexpr int SM_MASK = SM_P + 128 * 128;          // kStages x u64
-constexpr int SM_BAR = SM_MASK + 8 * kStages;
-enum Bar { KV_FULL = 0, KV_EMPTY = kStages, Q_FULL = 2 * kStages, S_FULL, S_FREE = S_FULL + 2, X_FULL = S_FREE + 2,
-           X_EMPTY = X_FULL + 2, P_FULL = X_EMPTY + 2, O_DONE, S_SUM, NBAR = S_SUM + 2 };
+constexpr int SM_STATE = SM_MASK + 8 * kStages;    // running max and sums, 128 heads x float4
+constexpr int SM_BAR = SM_STATE + 128 * 16;
+// S_FULL, X_FULL, X_EMPTY, ST_FULL and O_DONE come in pairs indexed by block parity:
+// each is then waited on only by one group, one phase at a time
+enum Bar { KV_FULL = 0, KV_EMPTY = kStages, Q_FULL = 2 * kStages, S_FULL, S_FREE = S_FULL + 2, X_FULL,
+           X_EMPTY = X_FULL + 2, ST_FULL = X_EMPTY + 2, P_FULL = ST_FULL + 2, O_DONE, NBAR = O_DONE + 2 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 4;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -70,10 +72,13 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the exchange scratch is indexed by SM");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_O = 0;            // 256 columns
-constexpr uint32_t TM_S = 256;          // 2 x 64 columns
+constexpr uint32_t TM_O = 0;            // O: 256 columns
+constexpr uint32_t TM_S = 256;          // partial then full scores of one block: 64 columns
+constexpr uint32_t TM_Q = 320;          // this CTA's q slice, bf16 pairs: 128 | 160 columns
+static_assert(SM_P % 1024 == 0, "swizzle atoms");
 
 struct TcFwdParams {
+  const uint16_t* q;                    // [T, 128, 576] bf16
   const uint16_t* kv;                   // [T, 576] bf16
   float* xchg;                          // exchange scratch, kXchgSlots slots
   const int32_t* indices;
@@ -87,7 +92,7 @@ struct TcFwdParams {
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
-    tc_fwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, TcFwdParams p) {
+    tc_fwd_h128_kernel(TcFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned (128B swizzle atoms)
   const uint32_t sb = smem_u32(smem);
@@ -106,19 +111,19 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       mbar_init(bar_addr(sb, KV_FULL + k), kProducers + 1);   // cp.async arrivals + the slot mask
       mbar_init(bar_addr(sb, KV_EMPTY + k), 1);
     }
-    mbar_init(bar_addr(sb, Q_FULL), 1);
+    mbar_init(bar_addr(sb, Q_FULL), 256);       // both groups stored their part of q into TMEM
     mbar_init(bar_addr(sb, S_FULL + 0), 1);
     mbar_init(bar_addr(sb, S_FULL + 1), 1);
-    mbar_init(bar_addr(sb, S_FREE + 0), 128);   // softmax threads loaded the full scores
-    mbar_init(bar_addr(sb, S_FREE + 1), 128);
-    mbar_init(bar_addr(sb, S_SUM + 0), 128);    // exchange threads stored the full scores
-    mbar_init(bar_addr(sb, S_SUM + 1), 128);
+    mbar_init(bar_addr(sb, S_FREE), 128);       // a group loaded the partial scores into registers
+    mbar_init(bar_addr(sb, ST_FULL + 0), 128);  // the group wrote the running state after its block
+    mbar_init(bar_addr(sb, ST_FULL + 1), 128);
     mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
     mbar_init(bar_addr(sb, X_FULL + 1), 128);
     mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
     mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
     mbar_init(bar_addr(sb, P_FULL), 128);
-    mbar_init(bar_addr(sb, O_DONE), 1);
+    mbar_init(bar_addr(sb, O_DONE + 0), 1);
+    mbar_init(bar_addr(sb, O_DONE + 1), 1);
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -135,12 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   if (warp < kProducers / 32) {
     // ------------------------------------------------------------ producers
     const int pt = threadIdx.x;              // 0..63
-    if (pt == 0) {
-      tma_prefetch_desc(&tm_q);
-      mbar_arrive_expect_tx(bar_addr(sb, Q_FULL), nch * kChunkQ);
-      for (int k = 0; k < nch; ++k)
-        tma_load_2d(sb + SM_Q + k * kChunkQ, &tm_q, 64 * (g0 + k), t * 128, bar_addr(sb, Q_FULL));
-    }
     // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
     const int c16 = pt & 7, r0 = pt >> 3;
     constexpr int RS = kProducers / 8;       // row stride between a thread's rows
@@ -185,67 +184,136 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Event driven: the score MMAs of block i are issued as soon as its KV stage
+    // has landed and its TMEM score buffer is free, the PV MMA of block j as soon
+    // as P(j) is written, whichever comes first.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
       const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
       // base descriptors; per-MMA descriptors only move the start address
-      const uint64_t dq0 = sdesc_sw128(sb + SM_Q, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sb + SM_KV, 16, 1024);
       const uint64_t dp0 = sdesc_sw128(sb + SM_P, 16, 1024);
       // V is the first four chunks of the stage, read MN-major:
       // LBO = stride between 64-dim chunks, SBO = stride between 8-row groups
       const uint64_t dv0 = sdesc_sw128(sb + SM_KV, kChunkKV, 1024);
       bool ok = mbar_wait(bar_addr(sb, Q_FULL), 0, abort_flag, p.status);
-      for (int i = 0; ok && i <= nblk; ++i) {
-        if (i < nblk) {
-          const int st = i % kStages, b = i & 1;
-          if (!mbar_wait(bar_addr(sb, KV_FULL + st), (i / kStages) & 1, abort_flag, p.status)) break;
-          if (i >= 2 && !mbar_wait(bar_addr(sb, S_FREE + b), ((i - 2) >> 1) & 1, abort_flag, p.status)) break;
-          fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
-          tc_fence_after();
+      tc_fence_after();
+      int ns = 0, npv = 0;                    // next block for the score MMAs / for PV
+      unsigned long long idle_since = 0;
+      while (ok && npv < nblk) {
+        bool progress = false;
+        if (ns < nblk) {
+          const int st = ns % kStages;
+          if (mbar_try_wait(bar_addr(sb, KV_FULL + st), (ns / kStages) & 1) &&
+              (ns < 1 || mbar_try_wait(bar_addr(sb, S_FREE), (ns - 1) & 1))) {
+            fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 5; ++k) {
-            if (k < nch) {
+            for (int k = 0; k < 5; ++k) {
+              if (k < nch) {
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ss(tmem + TM_S + 64 * b, sdesc_add(dq0, k * kChunkQ + ks * 32),
-                            sdesc_add(dk0, st * kStageBytes + k * kChunkKV + ks * 32), idesc_s, (k | ks) != 0);
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_bf16_ts(tmem + TM_S, tmem + TM_Q + 32 * k + 8 * ks,
+                              sdesc_add(dk0, st * kStageBytes + k * kChunkKV + ks * 32), idesc_s, (k | ks) != 0);
+              }
             }
+            mma_commit(bar_addr(sb, S_FULL + (ns & 1)));
+            ++ns;
+            progress = true;
           }
-          mma_commit(bar_addr(sb, S_FULL + b));
         }
-        if (i >= 1) {
-          const int j = i - 1, stj = j % kStages;
-          if (!mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status)) break;
+        if (npv < ns && mbar_try_wait(bar_addr(sb, P_FULL), npv & 1)) {
+          const int stj = npv % kStages;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16_ss(tmem + TM_O, sdesc_add(dp0, ks * 32), sdesc_add(dv0, stj * kStageBytes + ks * 16 * 128),
-                        idesc_pv, (j > 0 || ks > 0));
-          mma_commit(bar_addr(sb, O_DONE));
+                        idesc_pv, (npv > 0 || ks > 0));
+          mma_commit(bar_addr(sb, O_DONE + (npv & 1)));
           mma_commit(bar_addr(sb, KV_EMPTY + stj));
+          ++npv;
+          progress = true;
+        }
+        if (progress) {
+          idle_since = 0;
+        } else if (*abort_flag) {
+          break;
+        } else {
+          const unsigned long long now = globaltimer();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0u, kErrWaitTimeout);
+            break;
+          }
         }
       }
     }
     __syncwarp();
-  } else if (warp < kXchgWarp0) {
-    // ------------------------------------------------------------ softmax
+  } else {
+    // ------------------------------------------------------------ exchange + softmax
+    // Two groups of four warps take alternate blocks (group g: blocks i = g mod 2)
+    // so that one group's score exchange overlaps the other's softmax.  The
+    // running max and the two sums pass from group to group through shared
+    // memory, in block order.
+    const int g = (warp - kGroup0) >> 2;
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int h = 32 * q4 + lane;            // head == TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     uint8_t* prow = smem + SM_P + h * 128;
+    volatile float* state = reinterpret_cast<volatile float*>(smem + SM_STATE) + 4 * h;
+    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    // exchange slots of this CTA's SM and of the peer's SM
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
+    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
     // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
     float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
+    // this CTA's q slice into TMEM (the A operand of the score MMAs): head h in
+    // lane h, dims packed two per column; group g stores chunks g, g+2, ...
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * 128 + h) * kDqk + 64 * g0);
+      for (int k = g; k < nch; k += 2) {
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = __ldg(qrow + 8 * k + c);
+        tmem_st32(tl + TM_Q + 32 * k, reinterpret_cast<const float*>(v));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, Q_FULL));
+    }
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
-      const int b = i & 1, st = i % kStages;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM + b), (i >> 1) & 1, abort_flag, p.status)))) break;
+    for (int i = g; i < nblk; i += 2) {
+      const int b = g, st = i % kStages, k2 = i >> 1;
+      // own partial scores; the TMEM buffer is free again once they are in registers
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), k2 & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[64];
-      tmem_ld64(tl + TM_S + 64 * b, s);     // full scores (own + peer partials)
+      tmem_ld64(tl + TM_S, s);
       tc_fence_before();
-      mbar_arrive(bar_addr(sb, S_FREE + b));
+      mbar_arrive(bar_addr(sb, S_FREE));
+      // publish them to the peer, then add the peer's
+      if (k2 >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + b), (k2 - 1) & 1, abort_flag,
+                                                                   p.status))))
+        break;
+      float4* wr = xmine + b * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(s[4 * v4], s[4 * v4 + 1], s[4 * v4 + 2], s[4 * v4 + 3]);
+      mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), k2 & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + b * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v4 = 0; v4 < 16; ++v4) {
+        const float4 o = ld_cg_v4(rd + v4 * 128);
+        s[4 * v4] += o.x; s[4 * v4 + 1] += o.y; s[4 * v4 + 2] += o.z; s[4 * v4 + 3] += o.w;
+      }
+      mbar_arrive_remote(xempty_peer + 8 * b);    // the peer may reuse that buffer
       // slot validity of this block (written by the producer before it armed KV_FULL)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i / kStages) & 1, abort_flag, p.status)))) break;
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
@@ -254,6 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       for (int j = 0; j < 64; ++j) {
         s[j] = ((mask >> j) & 1ull) ? s[j] * p.c2 : -INFINITY;
         mx = fmaxf(mx, s[j]);
+      }
+      // running state after block i-1, from the other group
+      if (i >= 1) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, ST_FULL + (g ^ 1)), ((i - 1) >> 1) & 1, abort_flag,
+                                                     p.status))))
+          break;
+        m_run = state[0]; l = state[1]; l_bf = state[2];
       }
       // lazily updated running max: move it only when the block max exceeds it by > 8 (log2 units)
       const bool move = mx > m_run + kLazyRescale;
@@ -274,8 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       l = l * alpha + sum;
       l_bf = l_bf * alpha + sum_bf;
       m_run = m_new;
+      state[0] = m_run; state[1] = l; state[2] = l_bf;
+      mbar_arrive(bar_addr(sb, ST_FULL + g));
       // P buffer and O are free once the previous PV has completed
-      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (i - 1) & 1, abort_flag, p.status)))) break;
+      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + (b ^ 1)), ((i - 1) >> 1) & 1, abort_flag,
+                                                             p.status))))
+        break;
       tc_fence_after();
       if (i >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
@@ -297,9 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
     }
-    if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE), (nblk - 1) & 1, abort_flag, p.status));
+    // the group that took the last block holds the final state and writes the outputs
+    const bool last = (nblk == 0) ? (g == 0) : (g == ((nblk - 1) & 1));
+    if (ok && last && nblk > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1, abort_flag,
+                                             p.status));
     tc_fence_after();
-    if (ok) {
+    if (ok && last) {
       const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
       uint16_t* orow = p.out + ((int64_t)t * 128 + h) * kDv + 256 * crank;
 #pragma unroll 1
@@ -313,52 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
                               pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
       }
       if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
-    }
-      } else {
-    // ------------------------------------------------------------ exchange
-    const int q4 = warp & 3;
-    const int h = 32 * q4 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
-    // exchange slots of this CTA's SM and of the peer's SM
-    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
-    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
-    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    float cur[64];
-    // load block j's partial scores and publish them to the peer
-    auto publish = [&](int j, float* v) -> bool {
-      const int b = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), (j >> 1) & 1, abort_flag, p.status))) return false;
-      tc_fence_after();
-      tmem_ld64(tl + TM_S + 64 * b, v);
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + b), ((j >> 1) - 1) & 1, abort_flag,
-                                                              p.status)))
-        return false;
-      float4* wr = xmine + b * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
-      mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
-      return true;
-    };
-    bool ok = true;
-    for (int i = 0; ok && i < nblk; ++i) {
-      const int b = i & 1;
-      if (!(ok = publish(i, cur))) break;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), (i >> 1) & 1, abort_flag, p.status))))
-        break;
-      const float4* rd = xpeer + b * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v4 = 0; v4 < 16; ++v4) {
-        const float4 o = ld_cg_v4(rd + v4 * 128);
-        cur[4 * v4] += o.x; cur[4 * v4 + 1] += o.y; cur[4 * v4 + 2] += o.z; cur[4 * v4 + 3] += o.w;
-      }
-      mbar_arrive_remote(xempty_peer + 8 * b);    // the peer may reuse that buffer
-      tmem_st64(tl + TM_S + 64 * b, cur);         // full scores for the softmax warps
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, S_SUM + b));
     }
   }
 
@@ -393,36 +430,6 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status) {
 // exchange scratch of the tensor-core kernels (16 MiB), one slot per SM
 __device__ __align__(256) float g_xchg[kXchgSlots * kXchgSlotFloats];
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// 2-D bf16 tensor [rows, 576] with a box of `box_rows` x 64 columns, 128B swizzle.
-bool make_map_576(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {576, rows};
-  cuuint64_t strides[1] = {576 * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 uint32_t* tc_status_ptr() {
@@ -454,16 +461,14 @@ cudaError_t launch_wait_selftest(cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
-  CUtensorMap tm_q;
-  if (!make_map_576(&tm_q, a.q, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
   uint32_t* status = tc_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   float* xchg = tc_xchg_ptr();
   if (!xchg) return cudaErrorInvalidSymbol;
-  TcFwdParams p{a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
-  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, p);
+  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
+  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
