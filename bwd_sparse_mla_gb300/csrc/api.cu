@@ -37,6 +37,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool supported_h(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
+// H = 128 runs the tensor-core kernels, up to their top-k limit
+bool use_tc(int H, int topk) { return H == 128 && topk <= smla::kTcMaxTopk; }
 
 // The kernels are built for sm_103a only; refuse any other device.
 int check_device() {
@@ -116,7 +118,7 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
   if (int r = check_device()) return r;
   smla::FwdArgs a{q, kv, indices, out, lse, T, H, topk, scale};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (H == 128) ? smla::launch_fwd_tc(a, s) : smla::launch_fwd_simt(a, s);
+  cudaError_t e = use_tc(H, topk) ? smla::launch_fwd_tc(a, s) : smla::launch_fwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_fwd launch");
   count_launches(1);
   return 0;
@@ -163,7 +165,7 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
-  e = (H == 128) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
   count_launches(1);
   if (dkv != nullptr) {
@@ -251,7 +253,7 @@ int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const sm
   e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
-  e = (H == 128) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd_noalloc launch");
   count_launches(1);
   if (dkv != nullptr) {

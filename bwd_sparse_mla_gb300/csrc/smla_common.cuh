@@ -15,6 +15,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // sum of exponentials floored at 1e-30).
 constexpr float kLseEmpty = -69.07755278982137f;
 constexpr float kSumexpFloor = 1e-30f;
+// Largest top-k the H = 128 tensor-core kernels take (their lists of non-empty
+// blocks live in shared memory); larger top-k runs the CUDA-core kernels.
+constexpr int kTcMaxTopk = 16384;
 
 struct FwdArgs {
   const uint16_t* q;        // [T, H, 576] bf16

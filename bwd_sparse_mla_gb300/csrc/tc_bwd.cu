@@ -60,7 +60,11 @@ constexpr int SM_DS = SM_P + 128 * 128;
 constexpr int SM_ROWS = SM_DS + 128 * 128;              // 2 x 32 int32
 constexpr int SM_DROWS = SM_ROWS + 2 * 32 * 4;          // drain warps' copies of the row list, 4 x 2 x 32 int32
 constexpr int SM_MASK = SM_DROWS + 4 * 2 * 32 * 4;      // 2 x u32
-constexpr int SM_BAR = SM_MASK + 8;
+constexpr int kMaxBlocks = kTcMaxTopk / kBK;
+constexpr int SM_BFLAG = SM_MASK + 8;                   // per block: holds a valid slot (u8)
+constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;         // blocks with a valid slot, in order (u16)
+constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;        // their number
+constexpr int SM_BAR = SM_NB + 8;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 9,
            P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, S_SUM = 15, NBAR = 16 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
@@ -141,6 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  // blocks that hold only padding contribute nothing and are skipped: list the
+  // others in order (both CTAs of the pair read the same indices and agree)
+  const int16_t* blist = reinterpret_cast<const int16_t*>(smem + SM_BLIST);
+  const int nb = build_block_list<kBK>(p.indices + (int64_t)t * p.topk, nblk, p.T, smem + SM_BFLAG,
+                                       reinterpret_cast<int16_t*>(smem + SM_BLIST), reinterpret_cast<int*>(smem + SM_NB));
 
   if (warp < kProducers / 32) {
     // ------------------------------------------------------------ producers
@@ -161,19 +170,23 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const uint16_t* kvc = p.kv + 64 * g0 + 8 * c16;
     int* srows = reinterpret_cast<int*>(smem + SM_ROWS);
     int nxt[kRowsPerProducer], nm = 0;
+    if (nb > 0) {
+      const int32_t* ib = irow + blist[0] * kBK;
 #pragma unroll
-    for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + r0 + RS * j);
-    if (warp == 0) nm = __ldg(irow + lane);
-    for (int i = 0; i < nblk; ++i) {
+      for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+      if (warp == 0) nm = __ldg(ib + lane);
+    }
+    for (int i = 0; i < nb; ++i) {
       const int st = i & 1;
       int cur[kRowsPerProducer];
 #pragma unroll
       for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
       const int cm = nm;
-      if (i + 1 < nblk) {                    // indices of the next block, one block ahead
+      if (i + 1 < nb) {                      // indices of the next block, one block ahead
+        const int32_t* ib = irow + blist[i + 1] * kBK;
 #pragma unroll
-        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + (i + 1) * kBK + r0 + RS * j);
-        if (warp == 0) nm = __ldg(irow + (i + 1) * kBK + lane);
+        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+        if (warp == 0) nm = __ldg(ib + lane);
       }
       if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag,
                                                        p.status)))
@@ -219,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       bool ok = mbar_wait(bar_addr(sb, QD_FULL), 0, abort_flag, p.status);
       // iteration i issues S/dP of block i, then dQ/dKV of block i-1, so the
       // score MMAs of the next block run while the softmax warps work
-      for (int i = 0; ok && i <= nblk; ++i) {
-        if (i < nblk) {
+      for (int i = 0; ok && i <= nb; ++i) {
+        if (i < nb) {
           const int st = i & 1;
           if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
           if (i >= 1 && !(ok = mbar_wait(bar_addr(sb, SDP_FREE), (i - 1) & 1, abort_flag, p.status))) break;
@@ -297,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     uint8_t* dsrow = smem + SM_DS + h * 128;
     const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
+    for (int i = 0; i < nb; ++i) {
       const int st = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM), i & 1, abort_flag, p.status)))) break;
       tc_fence_after();
@@ -336,15 +349,20 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
     }
-    if (ok && nblk > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nblk - 1) & 1, abort_flag, p.status));
+    if (ok && nb > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
     if (ok) {
       uint16_t* qrow = p.dq + ((int64_t)t * 128 + h) * kDqk + 256 * crank;
 #pragma unroll 1
       for (int part = 0; part < ndq / 64; ++part) {
         float o[64];
-        tmem_ld64(tl + TM_DQ + 64 * part, o);
+        if (nb > 0) {
+          tmem_ld64(tl + TM_DQ + 64 * part, o);
+        } else {                             // no valid slot: no MMA ever wrote dQ
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[c] = 0.f;
+        }
         uint4* dst = reinterpret_cast<uint4*>(qrow + 64 * part);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -401,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     };
 
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
+    for (int i = 0; i < nb; ++i) {
       // exchange block i: partial S / dP rows through L2, buffer i&1 of the SM slots
       const int xb = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
@@ -437,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       // then drain the previous block's dKV tiles
       if (i >= 1 && !(ok = drain(i - 1))) break;
     }
-    if (ok && nblk > 0) drain(nblk - 1);
+    if (ok && nb > 0) drain(nb - 1);
   }
 
   // ------------------------------------------------------------ teardown

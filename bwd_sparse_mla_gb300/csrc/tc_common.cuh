@@ -125,6 +125,39 @@ constexpr int kXchgSlots = 256;
 constexpr int kXchgBufFloats = 16 * 128 * 4;          // 32 KiB
 constexpr int kXchgSlotFloats = 2 * kXchgBufFloats;   // 64 KiB
 
+// Called by every thread of the CTA: lists, in order, the blocks of `bk` slots of
+// a token's index row that hold at least one valid slot (0 <= idx < T), into
+// `list`, and returns their number.  Uses `flag` (nblk bytes) and `count` in
+// shared memory; contains two __syncthreads.
+template <int bk>
+__device__ __forceinline__ int build_block_list(const int32_t* irow, int nblk, int T, uint8_t* flag, int16_t* list,
+                                                int* count) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int b = warp; b < nblk; b += nwarps) {
+    bool v = false;
+#pragma unroll
+    for (int c = 0; c < bk; c += 32) {
+      const int x = __ldg(irow + b * bk + c + lane);
+      v |= (x >= 0 && x < T);
+    }
+    const bool any = __any_sync(0xffffffffu, v);
+    if (lane == 0) flag[b] = any ? 1 : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int base = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {
+      const bool f = (b0 + lane < nblk) && flag[b0 + lane];
+      const uint32_t m = __ballot_sync(0xffffffffu, f);
+      if (f) list[base + __popc(m & ((1u << lane) - 1u))] = (int16_t)(b0 + lane);
+      base += __popc(m);
+    }
+    if (lane == 0) *reinterpret_cast<volatile int*>(count) = base;
+  }
+  __syncthreads();
+  return *reinterpret_cast<volatile int*>(count);
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -252,6 +285,18 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const float* v) {
       : "memory");
 }
 // 32 lanes x 32 bits, 32 consecutive columns per thread (load + wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(

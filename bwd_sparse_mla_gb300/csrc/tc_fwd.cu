@@ -52,6 +52,7 @@ constexpr int kThreads = kProducers + 32 + 128 + 128;
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
 constexpr int kStageBytes = 5 * kChunkKV;
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
+constexpr int kMaxBlocks = kTcMaxTopk / kBK;
 
 // shared memory map (offsets from a 1024-aligned base); Q lives in TMEM
 constexpr int kStages = 5;
@@ -59,7 +60,10 @@ constexpr int SM_KV = 0;                           // kStages stages
 constexpr int SM_P = SM_KV + kStages * kStageBytes;
 constexpr int SM_MASK = SM_P + 128 * 128;          // kStages x u64
 constexpr int SM_STATE = SM_MASK + 8 * kStages;    // running max and sums, 128 heads x float4
-constexpr int SM_BAR = SM_STATE + 128 * 16;
+constexpr int SM_BFLAG = SM_STATE + 128 * 16;      // per block: holds a valid slot (u8)
+constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;     // blocks with a valid slot, in order (u16)
+constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;    // their number
+constexpr int SM_BAR = SM_NB + 8;
 // S_FULL, X_FULL, X_EMPTY, ST_FULL and O_DONE come in pairs indexed by block parity:
 // each is then waited on only by one group, one phase at a time
 enum Bar { KV_FULL = 0, KV_EMPTY = kStages, Q_FULL = 2 * kStages, S_FULL, S_FREE = S_FULL + 2, X_FULL,
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   const int t = blockIdx.x >> 1;
   const int nch = 4 + (int)crank;                     // 64-dim key chunks of this CTA
   const int g0 = 4 * (int)crank;                      // first global chunk
-  const int nblk = p.topk / kBK;
+  const int nblk = p.topk / kBK;           // blocks of the token's slot list
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
 
   if (threadIdx.x == 0) {
@@ -136,6 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   cluster_sync();   // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  // blocks that hold only padding contribute nothing and are skipped: list the
+  // others in order (both CTAs of the pair read the same indices and agree)
+  const int16_t* blist = reinterpret_cast<const int16_t*>(smem + SM_BLIST);
+  const int nb = build_block_list<kBK>(p.indices + (int64_t)t * p.topk, nblk, p.T, smem + SM_BFLAG,
+                                  reinterpret_cast<int16_t*>(smem + SM_BLIST), reinterpret_cast<int*>(smem + SM_NB));
 
   if (warp < kProducers / 32) {
     // ------------------------------------------------------------ producers
@@ -146,19 +155,23 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int32_t* irow = p.indices + (int64_t)t * p.topk;
     const uint16_t* kvc = p.kv + 64 * g0 + 8 * c16;
     int nxt[kRowsPerProducer], nm[2];
+    if (nb > 0) {
+      const int32_t* ib = irow + blist[0] * kBK;
 #pragma unroll
-    for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + r0 + RS * j);
-    if (warp == 0) { nm[0] = __ldg(irow + lane); nm[1] = __ldg(irow + 32 + lane); }
-    for (int i = 0; i < nblk; ++i) {
+      for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+      if (warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
+    }
+    for (int i = 0; i < nb; ++i) {
       const int st = i % kStages, use = i / kStages;
       int cur[kRowsPerProducer], cm[2];
 #pragma unroll
       for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
       cm[0] = nm[0]; cm[1] = nm[1];
-      if (i + 1 < nblk) {                    // indices of the next block, one block ahead
+      if (i + 1 < nb) {                      // indices of the next block, one block ahead
+        const int32_t* ib = irow + blist[i + 1] * kBK;
 #pragma unroll
-        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(irow + (i + 1) * kBK + r0 + RS * j);
-        if (warp == 0) { nm[0] = __ldg(irow + (i + 1) * kBK + lane); nm[1] = __ldg(irow + (i + 1) * kBK + 32 + lane); }
+        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+        if (warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
       }
       if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), (use - 1) & 1, abort_flag,
                                                         p.status)))
@@ -200,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_after();
       int ns = 0, npv = 0;                    // next block for the score MMAs / for PV
       unsigned long long idle_since = 0;
-      while (ok && npv < nblk) {
+      while (ok && npv < nb) {
         bool progress = false;
-        if (ns < nblk) {
+        if (ns < nb) {
           const int st = ns % kStages;
           if (mbar_try_wait(bar_addr(sb, KV_FULL + st), (ns / kStages) & 1) &&
               (ns < 1 || mbar_try_wait(bar_addr(sb, S_FREE), (ns - 1) & 1))) {
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       mbar_arrive(bar_addr(sb, Q_FULL));
     }
     bool ok = true;
-    for (int i = g; i < nblk; i += 2) {
+    for (int i = g; i < nb; i += 2) {
       const int b = g, st = i % kStages, k2 = i >> 1;
       // own partial scores; the TMEM buffer is free again once they are in registers
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), k2 & 1, abort_flag, p.status)))) break;
@@ -377,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       mbar_arrive(bar_addr(sb, P_FULL));
     }
     // the group that took the last block holds the final state and writes the outputs
-    const bool last = (nblk == 0) ? (g == 0) : (g == ((nblk - 1) & 1));
-    if (ok && last && nblk > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1, abort_flag,
+    const bool last = (nb == 0) ? (g == 0) : (g == ((nb - 1) & 1));
+    if (ok && last && nb > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1, abort_flag,
                                              p.status));
     tc_fence_after();
     if (ok && last) {
@@ -388,7 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 #pragma unroll 1
       for (int part = 0; part < 8; ++part) {
         float o[32];
-        tmem_ld32(tl + TM_O + 32 * part, o);
+        if (nb > 0) {
+          tmem_ld32(tl + TM_O + 32 * part, o);
+        } else {                             // no valid slot: no PV ever wrote O
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+        }
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * part);
 #pragma unroll
         for (int c = 0; c < 4; ++c)

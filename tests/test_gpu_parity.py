@@ -12,10 +12,25 @@ import torch
 import oracle.sparse_mla_ref as orc
 from bwd_sparse_mla_gb300 import capi
 from bwd_sparse_mla_gb300 import workloads as W
-from tests.gpu_helpers import (LSE_EMPTY_F32, assert_close, device_inputs, empty_rows,
+from tests.gpu_helpers import (LSE_EMPTY_F32, MAX_ABS, assert_close, device_inputs, empty_rows,
                                f64_to_bf16_dev, oracle_inputs, to_f64)
 
 pytestmark = pytest.mark.gpu
+
+def _with_padding_holes(w, seed):
+    """Moves each row's valid slots to random positions outside 64-slot blocks 1, 4 and 6, so
+    that whole blocks of padding sit between valid ones (the kernels skip such blocks)."""
+    rng = np.random.default_rng(seed)
+    idx = w.indices.reshape(w.T, w.topk)
+    out = np.full_like(idx, -1)
+    allowed = np.array([c for c in range(w.topk) if c // 64 not in (1, 4, 6)])
+    for r in range(w.T):
+        v = idx[r][idx[r] >= 0]
+        v = v[: allowed.size]
+        out[r, np.sort(rng.choice(allowed, v.size, replace=False))] = v
+    w.indices = out.reshape(w.T, 1, w.topk)
+    return w
+
 
 SMALL = {
     "cfg1-tiny": lambda: W.make_workload(1),
@@ -26,6 +41,10 @@ SMALL = {
     "ragged-H64": lambda: W.make_custom(640, 64, 256, [320, 320], seed=14, empty_rows=2),
     "ragged-H128-bigq": lambda: W.make_custom(520, 128, 320, [8, 200, 312], seed=15, empty_rows=3,
                                               q_std=8.0),
+    # whole blocks of padding between valid slots
+    "holes-H128": lambda: _with_padding_holes(W.make_custom(600, 128, 512, [600], seed=16, empty_rows=2), 16),
+    # top-k above the tensor-core kernels' limit (runs the CUDA-core kernels at H = 128)
+    "bigtopk-H128": lambda: W.make_custom(260, 128, 16448, [260], seed=17, empty_rows=2),
 }
 
 
@@ -83,12 +102,20 @@ def test_fwd_bwd_chain_small(small):
         pytest.skip("q ~ N(0, 8^2): the near one-hot softmax makes dS = P (dP - Delta) cancel, so the "
                     "chained dq inherits the forward's bf16 output rounding; the backward alone is "
                     "checked on identical inputs in test_bwd_small")
+    out_bf16 = torch.tensor(out_ref, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, out_bf16, dout, lse_ref, w.indices, w.scale)
+    # how far the bf16 rounding of `out` alone moves the oracle's own gradients: where kv rows
+    # are named by hundreds of queries this exceeds the bound, and no comparison through the
+    # bf16 `out` of the interface can then be held to it
+    dq_x, dkv_x = orc.sparse_mla_bwd(q, kv, out_ref, dout, lse_ref, w.indices, w.scale)
+    own = max(float((np.abs(a - b) / np.maximum(1.0, np.abs(b))).max()) for a, b in ((dq_x, dq_ref), (dkv_x, dkv_ref)))
+    if own > MAX_ABS:
+        pytest.skip(f"rounding `out` to bf16 moves the oracle's own dq/dkv by {own:.2e} (relative to max(1, |ref|)), "
+                    f"more than the {MAX_ABS} bound; the backward alone is checked in test_bwd_small")
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
     dq, dkv32, _ = capi.sparse_mla_bwd(d["q"], d["kv"], out, d["dout"], lse, d["indices"],
                                        d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
-    out_bf16 = torch.tensor(out_ref, dtype=torch.float64).to(torch.bfloat16).double().numpy()
-    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, out_bf16, dout, lse_ref, w.indices, w.scale)
     assert_close("dq(chain)", to_f64(dq), dq_ref)
     assert_close("dkv(chain)", to_f64(dkv32).reshape(w.T, -1), dkv_ref)
 
