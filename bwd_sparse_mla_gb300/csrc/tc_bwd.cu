@@ -25,10 +25,11 @@
 //   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
 //              transposed dKV tiles dKV^T[d, j] = dO^T (hi + lo) + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
-//   drain    : the exchange warps also read the dKV tiles from TMEM and add them into the
-//              fp32 dKV rows named by the valid slots (coalesced 128-byte
-//              fp32 reductions; padding slots issue no write, the no-op the
-//              miles PR #2079 summary describes for the clamped atomic).
+//   drain    : the exchange warps (slot columns 0..15) and the softmax warps
+//              (16..31) read the previous block's dKV tiles from TMEM and add
+//              them into the fp32 dKV rows named by the valid slots (coalesced
+//              128-byte fp32 reductions; padding slots issue no write, the
+//              no-op the miles PR #2079 summary describes for the clamped atomic).
 #include <cuda.h>
 
 #include "smla_common.cuh"
@@ -40,9 +41,9 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 32;
-constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax, w7..10 exchange + dKV drain
+constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax + drain, w7..10 exchange + drain
 constexpr int kMmaWarp = 2;
-constexpr int kDrainWarp0 = 7;
+constexpr int kXchgWarp0 = 7;
 constexpr int kThreads = 352;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4
 constexpr int kChunk = 128 * 128;       // 64-dim chunk of q / dO for 128 heads
@@ -58,8 +59,7 @@ constexpr int SM_KV = SM_DO + 4 * kChunk;               // 2 stages
 constexpr int SM_P = SM_KV + 2 * kStage;
 constexpr int SM_DS = SM_P + 128 * 128;
 constexpr int SM_ROWS = SM_DS + 128 * 128;              // 2 x 32 int32
-constexpr int SM_DROWS = SM_ROWS + 2 * 32 * 4;          // drain warps' copies of the row list, 4 x 2 x 32 int32
-constexpr int SM_MASK = SM_DROWS + 4 * 2 * 32 * 4;      // 2 x u32
+constexpr int SM_MASK = SM_ROWS + 2 * 32 * 4;           // 2 x u32
 constexpr int kMaxBlocks = kTcMaxTopk / kBK;
 constexpr int SM_BFLAG = SM_MASK + 8;                   // per block: holds a valid slot (u8)
 constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;         // blocks with a valid slot, in order (u16)
@@ -95,6 +95,38 @@ struct TcBwdParams {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
+
+// Adds half `half` (16 of the 32 slot columns) of block j's dKV^T tiles into the
+// fp32 rows the valid slots name.  `rows`: lane k holds the row of slot k (-1 for
+// padding).  Dims of tile m: CTA 0 -> [0,128), [128,256), tail [512,576);
+// CTA 1 -> [256,384), [384,512).  Called by a full set of four warps (one per
+// TMEM lane quarter); each thread arrives once per block on the DKV_FREE barrier.
+__device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int half,
+                                           int ntile, uint32_t crank, int L, float* dkv32, volatile int* abort_flag,
+                                           uint32_t* status) {
+  if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, status))) return false;
+  tc_fence_after();
+#pragma unroll 1
+  for (int m = 0; m < ntile; ++m) {
+    float gh[16], gl[16];
+    tmem_ld16(tl + tm_dkv + 64 * m + 16 * half, gh);        // hi half of the slots' columns
+    tmem_ld16(tl + tm_dkv + 64 * m + 32 + 16 * half, gl);   // lo half
+    if (m == ntile - 1) {               // this set's part of every tile is read: the MMA may overwrite them
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, DKV_FREE));
+    }
+    const int d = (crank == 0 ? (m < 2 ? 128 * m : 512) : 256 + 128 * m) + L;
+    if (d < kDqk) {                     // warp-uniform: only CTA 0's tail tile has lanes past 576
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int row = __shfl_sync(0xffffffffu, rows, 16 * half + k);
+        if (row >= 0) red_add_f32(dkv32 + (int64_t)row * kDqk + d, gh[k] + gl[k]);
+      }
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        TcBwdParams p) {
@@ -119,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     *abort_flag = 0;
     mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + mask/rows
     mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
-    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 128);   // MMA commit + drain threads (row list read)
-    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 128);
+    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 256);   // MMA commit + softmax and exchange threads (mask / rows read)
+    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 256);
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FREE), 128);
@@ -131,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
-    mbar_init(bar_addr(sb, DKV_FREE), 128);
+    mbar_init(bar_addr(sb, DKV_FREE), 256);      // both warp sets loaded their half of the tiles
     mbar_init(bar_addr(sb, S_SUM), 128);        // full S / dP stored back into TMEM
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
@@ -299,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
     }
     __syncwarp();
-  } else if (warp < kDrainWarp0) {
+  } else if (warp < kXchgWarp0) {
     // ------------------------------------------------------------ softmax / dS
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
@@ -310,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     uint8_t* dsrow = smem + SM_DS + h * 128;
     const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
     bool ok = true;
+    int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
       const int st = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM), i & 1, abort_flag, p.status)))) break;
@@ -321,6 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       mbar_arrive(bar_addr(sb, SDP_FREE));
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
+      const int rows = reinterpret_cast<const int*>(smem + SM_ROWS)[st * 32 + lane];
+      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
       uint32_t pp[16], dd[16], dl2[16], pl[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -348,7 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
+      // second half of the previous block's dKV tiles (the exchange warps drain the first)
+      if (i >= 1 && !(ok = drain_half(sb, tl, TM_DKV, i - 1, prev_rows, 1, ntile, crank, h, p.dkv32, abort_flag, p.status)))
+        break;
+      prev_rows = rows;
     }
+    if (ok && nb > 0) ok = drain_half(sb, tl, TM_DKV, nb - 1, prev_rows, 1, ntile, crank, h, p.dkv32, abort_flag, p.status);
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
@@ -376,7 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
-    // dims of dKV tile m: CTA 0 -> [0,128), [128,256), tail [512,576); CTA 1 -> [256,384), [384,512)
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
     const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
@@ -384,41 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + L;
     const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + L;
 
-    // drain block j's dKV tiles into the fp32 rows its valid slots name
-    auto drain = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, p.status))) return false;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (j >> 1) & 1, abort_flag, p.status))) return false;
-      // keep a per-warp copy of the block's rows, so the stage can be refilled
-      int* drows = reinterpret_cast<int*>(smem + SM_DROWS) + ((warp - kDrainWarp0) * 2 + (j & 1)) * 32;
-      drows[lane] = srows[st * 32 + lane];
-      __syncwarp();
-      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      tc_fence_after();
-#pragma unroll 1
-      for (int m = 0; m < ntile; ++m) {
-        float g[32], glo[32];
-        tmem_ld32(tl + TM_DKV + 64 * m, g);          // hi half
-        tmem_ld32(tl + TM_DKV + 64 * m + 32, glo);   // lo half
-        if (m == ntile - 1) {               // every tile is in registers: the MMA may overwrite them
-          tc_fence_before();
-          mbar_arrive(bar_addr(sb, DKV_FREE));
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) g[k] += glo[k];
-        const int d = (crank == 0 ? (m < 2 ? 128 * m : 512) : 256 + 128 * m) + L;
-        if (d < kDqk) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int row = drows[k];
-            if (row >= 0) red_add_f32(p.dkv32 + (int64_t)row * kDqk + d, g[k]);
-          }
-        }
-      }
-      return true;
-    };
-
     bool ok = true;
+    int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
       // exchange block i: partial S / dP rows through L2, buffer i&1 of the SM slots
       const int xb = i & 1;
@@ -452,10 +458,17 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(sb, S_SUM));
-      // then drain the previous block's dKV tiles
-      if (i >= 1 && !(ok = drain(i - 1))) break;
+      // row list of block i (the softmax warps read it too), then the first half of
+      // the previous block's dKV tiles
+      const int st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
+      const int rows = srows[st * 32 + lane];
+      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
+      if (i >= 1 && !(ok = drain_half(sb, tl, TM_DKV, i - 1, prev_rows, 0, ntile, crank, L, p.dkv32, abort_flag, p.status)))
+        break;
+      prev_rows = rows;
     }
-    if (ok && nb > 0) drain(nb - 1);
+    if (ok && nb > 0) drain_half(sb, tl, TM_DKV, nb - 1, prev_rows, 0, ntile, crank, L, p.dkv32, abort_flag, p.status);
   }
 
   // ------------------------------------------------------------ teardown
