@@ -187,6 +187,9 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+MODE_NAMES = {0: "atomic", 1: "deterministic (index-sorted segmented reduction)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -224,14 +227,15 @@ def run_ours(args):
     dq = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
     dkv32 = torch.empty((T, 1, 576), dtype=torch.float32, device=dev)
     dkv = torch.empty((T, 1, 576), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk), 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk, args.dkv_mode), 256), dtype=torch.uint8,
+                     device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
         capi.sparse_mla_fwd(q, kv, idx, cu, w.scale, out=out, lse=lse)
-        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dq=dq, dkv_f32=dkv32, dkv=dkv,
-                            workspace=ws)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dkv_mode=args.dkv_mode, dq=dq, dkv_f32=dkv32,
+                            dkv=dkv, workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -251,8 +255,8 @@ def run_ours(args):
         ev[k][0].record(stream)
         capi.sparse_mla_fwd(q, kv, idx, cu, w.scale, out=out, lse=lse)
         ev[k][1].record(stream)
-        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dq=dq, dkv_f32=dkv32, dkv=dkv,
-                            workspace=ws)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dkv_mode=args.dkv_mode, dq=dq, dkv_f32=dkv32,
+                            dkv=dkv, workspace=ws)
         ev[k][2].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -302,6 +306,27 @@ def run_ours(args):
         roof["traffic"] = tr["dram_bytes_per_launch"]
         roof["traffic_note"] = tr["note"]
 
+    # the other dKV mode, timed after the main region with the same L2 flush
+    other = None
+    if args.other_mode_steps > 0:
+        omode = 1 - args.dkv_mode
+        ws_o = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk, omode), 256), dtype=torch.uint8,
+                           device=dev)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dkv_mode=omode, dq=dq, dkv_f32=dkv32, dkv=dkv,
+                            workspace=ws_o)
+        oev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.other_mode_steps)]
+        for k in range(args.other_mode_steps):
+            flush.zero_()
+            oev[k][0].record(stream)
+            capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dkv_mode=omode, dq=dq, dkv_f32=dkv32,
+                                dkv=dkv, workspace=ws_o)
+            oev[k][1].record(stream)
+        torch.cuda.synchronize()
+        o_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in oev]))
+        other = {"dkv_mode": MODE_NAMES[omode], "ms": o_ms, "tflops": bwd_flop / (o_ms * 1e-3) / 1e12,
+                 "workspace_bytes": int(ws_o.numel()), "steps": args.other_mode_steps}
+        del ws_o
+
     e2e = None
     if rank == 0 or world > 1:
         e2e = run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu)
@@ -328,8 +353,9 @@ def run_ours(args):
             "fwd": {"ms": fwd_ms, "tflops": fwd_flop / (fwd_ms * 1e-3) / 1e12,
                     "roofline_frac": bound_ms(fwd_flop) / fwd_ms},
             "bwd": {"ms": bwd_ms, "tflops": bwd_flop / (bwd_ms * 1e-3) / 1e12,
-                    "roofline_frac": bound_ms(bwd_flop) / bwd_ms,
+                    "roofline_frac": bound_ms(bwd_flop) / bwd_ms, "dkv_mode": MODE_NAMES[args.dkv_mode],
                     "dkv_scatter_bytes": DKV_RED_BYTES_PER_SLOT * n_valid},
+            "bwd_other_dkv_mode": other,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -390,7 +416,7 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
         idx = hidx.to(dev, non_blocking=True)
         cu = hcu.to(dev, non_blocking=True)
         out, lse = capi.sparse_mla_fwd(q, kv, idx, cu, w.scale)
-        dq, _, dkv = capi.sparse_mla_bwd(q, kv, out, do, lse, idx, cu, w.scale)
+        dq, _, dkv = capi.sparse_mla_bwd(q, kv, out, do, lse, idx, cu, w.scale, dkv_mode=args.dkv_mode)
         o_out.copy_(out, non_blocking=True)
         o_lse.copy_(lse, non_blocking=True)
         o_dq.copy_(dq, non_blocking=True)
@@ -424,6 +450,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dkv-mode", type=int, default=0, choices=[0, 1],
+                    help="dKV accumulation of the timed backward: 0 = fp32 atomics, 1 = sorted segmented reduction")
+    ap.add_argument("--other-mode-steps", type=int, default=2,
+                    help="after the timed region, time the backward in the other dKV mode for this many steps")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -72,6 +72,37 @@ int check_shape(int T, int H, int topk, float scale) {
   } while (0)
 
 size_t delta_bytes(int T, int H) { return (((size_t)T * H * sizeof(float)) + 255) & ~(size_t)255; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the deterministic dKV mode: Delta, the per-row slot lists (CSR:
+// offset, fill cursor, reduction cursor, scan scratch, sorted slot ids) and the
+// per-slot contributions of one chunk of tokens.
+struct DetLayout {
+  size_t offset, cursor, pos, sums, seg, g;   // byte offsets
+  size_t per_token;                           // contribution bytes per token of a chunk
+  int ng;                                     // head groups per token (contributions per slot)
+};
+constexpr size_t kDetChunkBytes = size_t(4) << 30;   // default chunk: 4 GiB of contributions
+
+DetLayout det_layout(int T, int H, int topk) {
+  DetLayout L;
+  L.ng = use_tc(H, topk) ? 1 : smla::simt_head_groups(H);
+  size_t at = delta_bytes(T, H);
+  L.offset = at; at += align256(sizeof(int) * ((size_t)T + 1));
+  L.cursor = at; at += align256(sizeof(int) * (size_t)T);
+  L.pos = at;    at += align256(sizeof(int) * (size_t)T);
+  L.sums = at;   at += align256(sizeof(int) * (size_t)smla::det_scan_tiles(T));
+  L.seg = at;    at += align256(sizeof(int) * (size_t)T * topk);
+  L.g = at;
+  L.per_token = (size_t)L.ng * topk * smla::kDqk * sizeof(float);
+  return L;
+}
+size_t det_default_tokens(int T, const DetLayout& L) {
+  size_t tc = kDetChunkBytes / L.per_token;
+  if (tc < 1) tc = 1;
+  if (tc > (size_t)T) tc = (size_t)T;
+  return tc;
+}
 
 }  // namespace
 
@@ -126,8 +157,10 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
 
 size_t sparse_mla_bwd_workspace_bytes(int T, int H, int topk, int dkv_mode) {
   if (T < 0 || !supported_h(H) || topk <= 0 || topk % 64 != 0) return 0;
-  if (dkv_mode != SMLA_DKV_ATOMIC) return 0;
-  return delta_bytes(T, H);
+  if (dkv_mode == SMLA_DKV_ATOMIC) return delta_bytes(T, H);
+  if (dkv_mode != SMLA_DKV_DETERMINISTIC || (int64_t)T * topk > INT32_MAX) return 0;
+  const DetLayout L = det_layout(T, H, topk);
+  return L.g + det_default_tokens(T, L) * L.per_token;
 }
 
 int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
@@ -139,9 +172,10 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   (void)B;
   g_last_error.clear();
   if (int r = check_shape(T, H, topk, scale)) return r;
-  if (dkv_mode == SMLA_DKV_DETERMINISTIC)
-    return fail(-ENOTSUP, "dkv_mode SMLA_DKV_DETERMINISTIC is not built");
-  if (dkv_mode != SMLA_DKV_ATOMIC) return fail(-EINVAL, "unknown dkv_mode %d", dkv_mode);
+  if (dkv_mode != SMLA_DKV_ATOMIC && dkv_mode != SMLA_DKV_DETERMINISTIC)
+    return fail(-EINVAL, "unknown dkv_mode %d", dkv_mode);
+  if (dkv_mode == SMLA_DKV_DETERMINISTIC && (int64_t)T * topk > INT32_MAX)
+    return fail(-EINVAL, "SMLA_DKV_DETERMINISTIC needs T * topk <= 2^31 - 1 (got %lld)", (long long)T * topk);
   if (T == 0) return 0;
   SMLA_REQUIRE_PTR(q);
   SMLA_REQUIRE_PTR(kv);
@@ -153,7 +187,8 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   SMLA_REQUIRE_PTR(dkv_f32);
   if (dkv != nullptr && !aligned16(dkv)) return fail(-EINVAL, "dkv must be 16-byte aligned");
   SMLA_REQUIRE_PTR(workspace);
-  const size_t need = delta_bytes(T, H);
+  const DetLayout L = det_layout(T, H, topk);
+  const size_t need = dkv_mode == SMLA_DKV_ATOMIC ? delta_bytes(T, H) : L.g + L.per_token;
   if (workspace_bytes < need)
     return fail(-EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
   if (int r = check_device()) return r;
@@ -165,9 +200,38 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
-  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
-  count_launches(1);
+  if (dkv_mode == SMLA_DKV_ATOMIC) {
+    e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
+    count_launches(1);
+  } else {
+    // index-sorted segmented reduction: slot lists per kv row, then chunks of
+    // tokens whose per-slot contributions are added to their rows in slot order
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    int* offset = reinterpret_cast<int*>(w + L.offset);
+    int* pos = reinterpret_cast<int*>(w + L.pos);
+    int* seg = reinterpret_cast<int*>(w + L.seg);
+    float* gbuf = reinterpret_cast<float*>(w + L.g);
+    int nl = 0;
+    e = smla::launch_build_row_lists(indices, T, topk, offset, reinterpret_cast<int*>(w + L.cursor), pos, seg,
+                                     reinterpret_cast<int*>(w + L.sums), s, &nl);
+    if (e != cudaSuccess) return cuda_fail(e, "slot list launch");
+    count_launches(nl);
+    size_t tc = (workspace_bytes - L.g) / L.per_token;
+    if (tc > (size_t)T) tc = (size_t)T;
+    a.gbuf = gbuf;
+    a.gstride = (int64_t)tc * topk * smla::kDqk;
+    for (int t0 = 0; t0 < T; t0 += (int)tc) {
+      a.t0 = t0;
+      a.nt = (int)((size_t)(T - t0) < tc ? (size_t)(T - t0) : tc);
+      e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+      if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
+      e = smla::launch_reduce_rows(offset, seg, pos, gbuf, L.ng, a.gstride, (int64_t)t0 * topk,
+                                   (int64_t)(t0 + a.nt) * topk, T, dkv_f32, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dkv reduction launch");
+      count_launches(2);
+    }
+  }
   if (dkv != nullptr) {
     e = smla::launch_cast_bf16(dkv_f32, dkv, (int64_t)T * smla::kDqk, s);
     if (e != cudaSuccess) return cuda_fail(e, "dkv cast launch");

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_simt_kernel(BwdArgs a) {
   float* s_dl = s_lse2 + HG;                       // [HG]
   int* s_row = reinterpret_cast<int*>(s_dl + HG);  // [kBK]
 
-  const int t = blockIdx.x;
+  const int t = a.t0 + blockIdx.x;
   const int h0 = blockIdx.y * HG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float c2 = a.scale * kLog2e;
@@ -276,9 +276,16 @@ __global__ void __launch_bounds__(kNT, 1) bwd_simt_kernel(BwdArgs a) {
           }
         }
       }
-      float* dst = a.dkv32 + (int64_t)row * kDqk + kd0;
+      if (a.gbuf != nullptr) {           // deterministic mode: store this head group's part of the slot
+        float* dst = a.gbuf + (int64_t)blockIdx.y * a.gstride +
+                     ((int64_t)(t - a.t0) * a.topk + (int64_t)blk * kBK + kj) * kDqk + kd0;
 #pragma unroll
-      for (int n = 0; n < NK; ++n) red_add_v4(dst + 32 * n, g[n].x, g[n].y, g[n].z, g[n].w);
+        for (int n = 0; n < NK; ++n) *reinterpret_cast<float4*>(dst + 32 * n) = g[n];
+      } else {
+        float* dst = a.dkv32 + (int64_t)row * kDqk + kd0;
+#pragma unroll
+        for (int n = 0; n < NK; ++n) red_add_v4(dst + 32 * n, g[n].x, g[n].y, g[n].z, g[n].w);
+      }
     }
     __syncthreads();
   }
@@ -375,7 +382,9 @@ cudaError_t bwd_launch(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(bwd_simt_kernel<HG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  bwd_simt_kernel<HG><<<dim3(a.T, a.H / HG), kNT, sm, s>>>(a);
+  const int nt = a.nt < 0 ? a.T : a.nt;
+  if (nt == 0) return cudaSuccess;
+  bwd_simt_kernel<HG><<<dim3(nt, a.H / HG), kNT, sm, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -386,6 +395,8 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
   if (a.H == 16) return fwd_launch<16>(a, s);
   return fwd_launch<32>(a, s);  // H = 32, 64, 128 in groups of 32 heads
 }
+
+int simt_head_groups(int H) { return H <= 16 ? 1 : H / 32; }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
   if (a.H == 8) return bwd_launch<8>(a, s);

@@ -40,6 +40,13 @@ struct BwdArgs {
   float* dkv32;             // [T, 576] fp32 accumulator (zeroed before)
   int T, H, topk;
   float scale;
+  // token range [t0, t0 + nt) of this launch (nt < 0: all T tokens)
+  int t0 = 0, nt = -1;
+  // deterministic dKV: when gbuf != nullptr the kernels store each valid slot's
+  // contribution at gbuf + g * gstride + ((t - t0) * topk + j) * 576 (head group g)
+  // instead of adding it into dkv32
+  float* gbuf = nullptr;
+  int64_t gstride = 0;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -83,6 +90,14 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t read_tc_status(uint32_t* out, bool clear);
 cudaError_t launch_wait_selftest(cudaStream_t s);
+// deterministic dKV (dkv_det.cu)
+int64_t det_scan_tiles(int T);
+cudaError_t launch_build_row_lists(const int32_t* indices, int T, int topk, int* offset, int* cursor, int* pos,
+                                   int* seg, int* scan_sums, cudaStream_t s, int* nlaunch);
+cudaError_t launch_reduce_rows(const int* offset, const int* seg, int* pos, const float* gbuf, int ng,
+                               int64_t gstride, int64_t slot_lo, int64_t slot_hi, int T, float* dkv32,
+                               cudaStream_t s);
+int simt_head_groups(int H);   // CUDA-core backward: CTAs (head groups) per token
 cudaError_t launch_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
                                  int B, unsigned long long* counter, cudaStream_t s);
 

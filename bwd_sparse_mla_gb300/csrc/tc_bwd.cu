@@ -88,8 +88,9 @@ struct TcBwdParams {
   const float* delta;
   uint16_t* dq;
   float* dkv32;
+  float* gbuf;                          // deterministic mode: per-slot contributions of this launch's tokens
   uint32_t* status;
-  int T, topk;
+  int T, topk, t0;                      // this launch handles tokens t0, t0 + 1, ...
   float scale, c2;
 };
 
@@ -101,9 +102,12 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // padding).  Dims of tile m: CTA 0 -> [0,128), [128,256), tail [512,576);
 // CTA 1 -> [256,384), [384,512).  Called by a full set of four warps (one per
 // TMEM lane quarter); each thread arrives once per block on the DKV_FREE barrier.
+// With kStore (deterministic mode) the slot rows are stored at gslot + k * 576
+// (k = slot within the block) instead of added into dkv32.
+template <bool kStore>
 __device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int half,
-                                           int ntile, uint32_t crank, int L, float* dkv32, volatile int* abort_flag,
-                                           uint32_t* status) {
+                                           int ntile, uint32_t crank, int L, float* dkv32, float* gslot,
+                                           volatile int* abort_flag, uint32_t* status) {
   if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, status))) return false;
   tc_fence_after();
 #pragma unroll 1
@@ -120,11 +124,23 @@ __device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int row = __shfl_sync(0xffffffffu, rows, 16 * half + k);
-        if (row >= 0) red_add_f32(dkv32 + (int64_t)row * kDqk + d, gh[k] + gl[k]);
+        if (row < 0) continue;
+        if (kStore)
+          gslot[(16 * half + k) * kDqk + d] = gh[k] + gl[k];
+        else
+          red_add_f32(dkv32 + (int64_t)row * kDqk + d, gh[k] + gl[k]);
       }
     }
   }
   return true;
+}
+
+__device__ __forceinline__ bool drain_half_any(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int half,
+                                               int ntile, uint32_t crank, int L, float* dkv32, float* gslot,
+                                               volatile int* abort_flag, uint32_t* status) {
+  return gslot != nullptr
+             ? drain_half<true>(sb, tl, tm_dkv, j, rows, half, ntile, crank, L, dkv32, gslot, abort_flag, status)
+             : drain_half<false>(sb, tl, tm_dkv, j, rows, half, ntile, crank, L, dkv32, gslot, abort_flag, status);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
@@ -136,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
   const uint32_t peer = crank ^ 1u;
-  const int t = blockIdx.x >> 1;
+  const int t = p.t0 + (blockIdx.x >> 1);
   const int nch = 4 + (int)crank;          // key chunks (64 dims each) of this CTA
   const int g0 = 4 * (int)crank;           // first global key chunk; value chunks are g0 .. g0+3
   // q chunks held: the key chunks, and for CTA 0 also the rope tail (chunk 8) in slot 4,
@@ -180,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   // blocks that hold only padding contribute nothing and are skipped: list the
   // others in order (both CTAs of the pair read the same indices and agree)
   const int16_t* blist = reinterpret_cast<const int16_t*>(smem + SM_BLIST);
+  // deterministic mode: where the contributions of block j (of the list) go
+  auto gslot = [&](int j) -> float* {
+    return p.gbuf == nullptr ? nullptr : p.gbuf + ((int64_t)(t - p.t0) * p.topk + (int64_t)blist[j] * kBK) * kDqk;
+  };
   const int nb = build_block_list<kBK>(p.indices + (int64_t)t * p.topk, nblk, p.T, smem + SM_BFLAG,
                                        reinterpret_cast<int16_t*>(smem + SM_BLIST), reinterpret_cast<int*>(smem + SM_NB));
 
@@ -384,11 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
       // second half of the previous block's dKV tiles (the exchange warps drain the first)
-      if (i >= 1 && !(ok = drain_half(sb, tl, TM_DKV, i - 1, prev_rows, 1, ntile, crank, h, p.dkv32, abort_flag, p.status)))
+      if (i >= 1 && !(ok = drain_half_any(sb, tl, TM_DKV, i - 1, prev_rows, 1, ntile, crank, h, p.dkv32, gslot(i - 1),
+                                      abort_flag, p.status)))
         break;
       prev_rows = rows;
     }
-    if (ok && nb > 0) ok = drain_half(sb, tl, TM_DKV, nb - 1, prev_rows, 1, ntile, crank, h, p.dkv32, abort_flag, p.status);
+    if (ok && nb > 0)
+      ok = drain_half_any(sb, tl, TM_DKV, nb - 1, prev_rows, 1, ntile, crank, h, p.dkv32, gslot(nb - 1), abort_flag, p.status);
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
@@ -464,11 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const int rows = srows[st * 32 + lane];
       mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      if (i >= 1 && !(ok = drain_half(sb, tl, TM_DKV, i - 1, prev_rows, 0, ntile, crank, L, p.dkv32, abort_flag, p.status)))
+      if (i >= 1 && !(ok = drain_half_any(sb, tl, TM_DKV, i - 1, prev_rows, 0, ntile, crank, L, p.dkv32, gslot(i - 1),
+                                      abort_flag, p.status)))
         break;
       prev_rows = rows;
     }
-    if (ok && nb > 0) drain_half(sb, tl, TM_DKV, nb - 1, prev_rows, 0, ntile, crank, L, p.dkv32, abort_flag, p.status);
+    if (ok && nb > 0)
+      drain_half_any(sb, tl, TM_DKV, nb - 1, prev_rows, 0, ntile, crank, L, p.dkv32, gslot(nb - 1), abort_flag, p.status);
   }
 
   // ------------------------------------------------------------ teardown
@@ -525,8 +549,11 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   if (!status || !xchg) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  TcBwdParams p{a.kv, xchg, a.indices, a.lse, a.delta, a.dq, a.dkv32, status, a.T, a.topk, a.scale, a.scale * kLog2e};
-  tc_bwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
+  const int nt = a.nt < 0 ? a.T : a.nt;
+  if (nt == 0) return cudaSuccess;
+  TcBwdParams p{a.kv,   xchg,     a.indices, a.lse, a.delta, a.dq,  a.dkv32,
+                a.gbuf, status,   a.T,       a.topk, a.t0,  a.scale, a.scale * kLog2e};
+  tc_bwd_h128_kernel<<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }
 

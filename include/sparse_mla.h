@@ -61,8 +61,8 @@ typedef uint16_t smla_bf16_t;  /* bfloat16 bit pattern */
 
 #define SMLA_D_QK 576          /* 512 latent + 64 rope tail */
 #define SMLA_D_V 512           /* latent width = value width */
-#define SMLA_DKV_ATOMIC 0      /* dKV scatter by fp32 vector atomics */
-#define SMLA_DKV_DETERMINISTIC 1  /* reserved: sorted segmented reduction */
+#define SMLA_DKV_ATOMIC 0         /* dKV scatter by fp32 atomic adds (order varies run to run) */
+#define SMLA_DKV_DETERMINISTIC 1  /* dKV by an index-sorted segmented reduction (bitwise reproducible) */
 
 /* fp32 LSE written for a row with no valid slot: ln(1e-30) rounded to fp32
  * (the 1e-30 floor of the miles PR #2079 forward fragment, empty max read
@@ -87,8 +87,12 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
                    smla_bf16_t* out, float* lse, void* stream);
 
 /* Bytes of device workspace sparse_mla_bwd needs for these sizes (0 if the
- * sizes are invalid).  The workspace holds Delta = rowsum(dO * out), [T, H]
- * fp32, and is fully overwritten by each call. */
+ * sizes are invalid).  SMLA_DKV_ATOMIC: Delta = rowsum(dO * out), [T, H] fp32.
+ * SMLA_DKV_DETERMINISTIC: Delta, the kv rows' sorted slot lists (about
+ * 4 * (3 T + T * topk) bytes) and the per-slot dKV contributions of one chunk of
+ * query tokens (the default chunk holds 4 GiB of them; any workspace of at least
+ * one token's worth is accepted, and a smaller one only means more chunks).
+ * Fully overwritten by each call. */
 size_t sparse_mla_bwd_workspace_bytes(int T, int H, int topk, int dkv_mode);
 
 /*
@@ -98,7 +102,14 @@ size_t sparse_mla_bwd_workspace_bytes(int T, int H, int topk, int dkv_mode);
  *   out      [T, H, 512] bf16   forward output (used only for Delta)
  *   dout     [T, H, 512] bf16   gradient of the loss w.r.t. out
  *   lse      [T, H] fp32        forward LSE (natural log)
- *   dkv_mode SMLA_DKV_ATOMIC (SMLA_DKV_DETERMINISTIC returns -ENOTSUP)
+ *   dkv_mode SMLA_DKV_ATOMIC: each valid slot's dKV row is added into dkv_f32
+ *            with fp32 atomic adds, whose order (and so the last bits) varies
+ *            from run to run.
+ *            SMLA_DKV_DETERMINISTIC: the slots are first sorted by the kv row
+ *            they name; dkv_f32[r] is then the fp32 sum of row r's per-slot
+ *            contributions taken left to right in ascending slot order
+ *            (t * topk + j), the same bits on every run and for any workspace
+ *            size.  Needs T * topk <= 2^31 - 1.
  *   dq       [T, H, 576] bf16   gradient w.r.t. q; exactly 0 on empty rows
  *   dkv_f32  [T, 1, 576] fp32   gradient w.r.t. kv; zeroed and then
  *            scatter-added by this call (rows no valid slot names stay 0)

@@ -77,8 +77,10 @@ def _bwd(lib, T=16, H=8, topk=64, mode=0, ws=FAKE, ws_bytes=1 << 20, dq=FAKE):
 
 
 def test_bwd_rejects_bad_arguments(lib):
-    assert _bwd(lib, mode=1) == ENOTSUP
-    assert "DETERMINISTIC" in capi.sparse_mla_last_error()
+    assert _bwd(lib, mode=1, ws_bytes=4096) == EINVAL          # smaller than one token's contributions
+    assert "workspace too small" in capi.sparse_mla_last_error()
+    assert _bwd(lib, mode=1, T=1 << 20, topk=4096) == EINVAL   # slot ids must fit int32
+    assert "T * topk" in capi.sparse_mla_last_error()
     assert _bwd(lib, mode=7) == EINVAL
     assert _bwd(lib, ws_bytes=16) == EINVAL
     assert "workspace too small" in capi.sparse_mla_last_error()
@@ -92,7 +94,14 @@ def test_workspace_bytes(lib):
     assert capi.sparse_mla_bwd_workspace_bytes(1000, 128, 2048) >= 1000 * 128 * 4
     assert capi.sparse_mla_bwd_workspace_bytes(1000, 12, 2048) == 0
     assert capi.sparse_mla_bwd_workspace_bytes(1000, 8, 100) == 0
-    assert capi.sparse_mla_bwd_workspace_bytes(1000, 8, 64, 1) == 0
+    # deterministic mode: Delta, the slot lists (T * topk ints and more) and one chunk of
+    # per-slot contributions (all 1000 tokens fit in the default 4 GiB chunk here)
+    det = capi.sparse_mla_bwd_workspace_bytes(1000, 8, 64, 1)
+    assert det >= 1000 * 8 * 4 + 4 * 1000 * 64 + 1000 * 64 * 576 * 4
+    # the default chunk is capped: at the headline size it is 4 GiB of contributions
+    big = capi.sparse_mla_bwd_workspace_bytes(65536, 128, 2048, 1)
+    assert 4 << 30 <= big <= (4 << 30) + 65536 * 128 * 4 + 4 * (3 * 65536 + 65536 * 2048) + (1 << 20)
+    assert capi.sparse_mla_bwd_workspace_bytes(1 << 20, 8, 4096, 1) == 0
 
 
 def test_check_indices_rejects_bad_arguments(lib):

@@ -123,8 +123,9 @@ def test_fwd_bwd_chain_small(small):
 FULL_SAMPLE = {2: 512, 3: 512, 4: 384, 5: 256}
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_full_size_sampled(cfg, cuda_device):
+@pytest.mark.parametrize("cfg,dkv_mode", [(2, 0), (3, 0), (3, 1), (4, 0), (5, 0), (5, 1)],
+                         ids=["cfg2", "cfg3", "cfg3-deterministic", "cfg4", "cfg5", "cfg5-deterministic"])
+def test_full_size_sampled(cfg, dkv_mode, cuda_device):
     w = W.make_workload(cfg)
     rows = W.sample_rows(w, FULL_SAMPLE[cfg])
     d = device_inputs(w, cuda_device)
@@ -148,7 +149,7 @@ def test_full_size_sampled(cfg, cuda_device):
     dout_m = torch.zeros_like(d["dout"])
     dout_m[rt] = d["dout"][rt]
     dq, dkv32, _ = capi.sparse_mla_bwd(d["q"], d["kv"], out_in, dout_m, lse_in, d["indices"],
-                                       d["cu_seqlens"], w.scale, want_bf16_dkv=False)
+                                       d["cu_seqlens"], w.scale, dkv_mode=dkv_mode, want_bf16_dkv=False)
     torch.cuda.synchronize()
     dq_ref, dkv_ref = orc.sparse_mla_bwd(w.q, w.kv, to_f64(out_in[rt]), w.dout, to_f64(lse_in[rt]),
                                          w.indices, w.scale, rows=rows)
