@@ -37,8 +37,9 @@ int cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool supported_h(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H == 128; }
-// H = 128 runs the tensor-core kernels, up to their top-k limit
-bool use_tc(int H, int topk) { return H == 128 && topk <= smla::kTcMaxTopk; }
+// The tensor-core kernels take every supported H (a 128-row head tile, rows
+// past H zero) up to their top-k limit; larger top-k runs the CUDA-core kernels.
+bool use_tc(int H, int topk) { (void)H; return topk <= smla::kTcMaxTopk; }
 
 // The kernels are built for sm_103a only; refuse any other device.
 int check_device() {

@@ -1,4 +1,5 @@
-// Tensor-core (tcgen05) backward for H = 128 heads.
+// Tensor-core (tcgen05) backward for up to 128 heads (fewer heads run as a
+// 128-row tile whose rows past H are zero).
 //
 // Work split: as in the forward, a cluster of two CTAs handles one query
 // token and splits the feature dimension: CTA 0 owns key dims [0,256) and
@@ -90,7 +91,7 @@ struct TcBwdParams {
   float* dkv32;
   float* gbuf;                          // deterministic mode: per-slot contributions of this launch's tokens
   uint32_t* status;
-  int T, topk, t0;                      // this launch handles tokens t0, t0 + 1, ...
+  int T, H, topk, t0;                   // this launch handles tokens t0, t0 + 1, ...; H <= 128 heads
   float scale, c2;
 };
 
@@ -193,6 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  // fewer than 128 heads: rows H..127 of every q / dO chunk are zero (the
+  // MMAs read all 128 rows); the fence orders these stores before the MMAs
+  if (p.H < 128) {
+    const int per_chunk = (128 - p.H) * 8;      // 16-byte pieces
+    for (int i = threadIdx.x; i < 9 * per_chunk; i += kThreads) {
+      const int c = i / per_chunk, r = p.H + (i % per_chunk) / 8, piece = i % 8;
+      *reinterpret_cast<uint4*>(smem + SM_Q + c * kChunk + r * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   // blocks that hold only padding contribute nothing and are skipped: list the
   // others in order (both CTAs of the pair read the same indices and agree)
   const int16_t* blist = reinterpret_cast<const int16_t*>(smem + SM_BLIST);
@@ -207,13 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     // ------------------------------------------------------------ producers
     const int pt = threadIdx.x;              // 0..63
     if (pt == 0) {
+      // the token's H head rows of each 64-dim chunk; rows H..127 were zeroed above
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (5 + 4) * kChunk);
+      mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (5 + 4) * p.H * 128);
       for (int k = 0; k < 5; ++k)
-        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (k < nch ? g0 + k : 8), t * 128, bar_addr(sb, QD_FULL));
+        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (k < nch ? g0 + k : 8), t * p.H, bar_addr(sb, QD_FULL));
       for (int k = 0; k < 4; ++k)
-        tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * 128, bar_addr(sb, QD_FULL));
+        tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * p.H, bar_addr(sb, QD_FULL));
     }
     // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
     const int c16 = pt & 7, r0 = pt >> 3;
@@ -356,8 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const float lse2 = p.lse[(int64_t)t * 128 + h] * kLog2e;
-    const float dl = p.delta[(int64_t)t * 128 + h];
+    // heads past H: lse = +inf gives P = 0 and dS' = 0 exactly
+    const bool real = h < p.H;
+    const float lse2 = real ? p.lse[(int64_t)t * p.H + h] * kLog2e : INFINITY;
+    const float dl = real ? p.delta[(int64_t)t * p.H + h] : 0.f;
     uint8_t* prow = smem + SM_P + h * 128;
     uint8_t* dsrow = smem + SM_DS + h * 128;
     const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
     if (ok) {
-      uint16_t* qrow = p.dq + ((int64_t)t * 128 + h) * kDqk + 256 * crank;
+      uint16_t* qrow = p.dq + ((int64_t)t * p.H + h) * kDqk + 256 * crank;
 #pragma unroll 1
       for (int part = 0; part < ndq / 64; ++part) {
         float o[64];
@@ -426,10 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           for (int c = 0; c < 64; ++c) o[c] = 0.f;
         }
         uint4* dst = reinterpret_cast<uint4*>(qrow + 64 * part);
+        if (real) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
-                              pack_bf16x2(o[8 * c + 4], o[8 * c + 5]), pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
+                                pack_bf16x2(o[8 * c + 4], o[8 * c + 5]), pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+        }
       }
     }
   } else {
@@ -542,8 +558,8 @@ float* tc_xchg_ptr();
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap tm_q, tm_do;
-  if (!make_map(&tm_q, a.q, kDqk, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&tm_do, a.dout, kDv, (uint64_t)a.T * 128, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tm_q, a.q, kDqk, (uint64_t)a.T * a.H, a.H)) return cudaErrorInvalidValue;
+  if (!make_map(&tm_do, a.dout, kDv, (uint64_t)a.T * a.H, a.H)) return cudaErrorInvalidValue;
   uint32_t* status = tc_status_ptr();
   float* xchg = tc_xchg_ptr();
   if (!status || !xchg) return cudaErrorInvalidSymbol;
@@ -551,8 +567,8 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int nt = a.nt < 0 ? a.T : a.nt;
   if (nt == 0) return cudaSuccess;
-  TcBwdParams p{a.kv,   xchg,     a.indices, a.lse, a.delta, a.dq,  a.dkv32,
-                a.gbuf, status,   a.T,       a.topk, a.t0,  a.scale, a.scale * kLog2e};
+  TcBwdParams p{a.kv,   xchg,   a.indices, a.lse, a.delta, a.dq,    a.dkv32,
+                a.gbuf, status, a.T,       a.H,   a.topk,  a.t0,    a.scale, a.scale * kLog2e};
   tc_bwd_h128_kernel<<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }

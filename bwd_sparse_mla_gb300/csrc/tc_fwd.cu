@@ -1,4 +1,5 @@
-// Tensor-core (tcgen05) forward for H = 128 heads.
+// Tensor-core (tcgen05) forward for up to 128 heads (fewer heads run as a
+// 128-row tile whose rows past H are zero).
 //
 // Work split: a cluster of two CTAs handles one query token.  The 576-wide
 // key dimension is split between them (CTA 0: dims [0,256), CTA 1: dims
@@ -82,14 +83,14 @@ constexpr uint32_t TM_Q = 320;          // this CTA's q slice, bf16 pairs: 128 |
 static_assert(SM_P % 1024 == 0, "swizzle atoms");
 
 struct TcFwdParams {
-  const uint16_t* q;                    // [T, 128, 576] bf16
+  const uint16_t* q;                    // [T, H, 576] bf16
   const uint16_t* kv;                   // [T, 576] bf16
   float* xchg;                          // exchange scratch, kXchgSlots slots
   const int32_t* indices;
   uint16_t* out;
   float* lse;
   uint32_t* status;
-  int T, topk;
+  int T, H, topk;                       // H <= 128 heads; rows H..127 of the tile are zero
   float c2;                             // scale * log2(e)
 };
 
@@ -289,11 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     // this CTA's q slice into TMEM (the A operand of the score MMAs): head h in
     // lane h, dims packed two per column; group g stores chunks g, g+2, ...
     {
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * 128 + h) * kDqk + 64 * g0);
+      const bool real = h < p.H;             // heads past H are zero rows of the tile
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk + 64 * g0);
       for (int k = g; k < nch; k += 2) {
         uint4 v[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = __ldg(qrow + 8 * k + c);
+        for (int c = 0; c < 8; ++c) v[c] = real ? __ldg(qrow + 8 * k + c) : make_uint4(0u, 0u, 0u, 0u);
         tmem_st32(tl + TM_Q + 32 * k, reinterpret_cast<const float*>(v));
       }
       tmem_wait_st();
@@ -397,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_fence_after();
     if (ok && last) {
       const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
-      uint16_t* orow = p.out + ((int64_t)t * 128 + h) * kDv + 256 * crank;
+      const bool real = h < p.H;
+      uint16_t* orow = p.out + ((int64_t)t * p.H + h) * kDv + 256 * crank;
 #pragma unroll 1
       for (int part = 0; part < 8; ++part) {
         float o[32];
@@ -408,12 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           for (int c = 0; c < 32; ++c) o[c] = 0.f;
         }
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * part);
+        if (real) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                              pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        }
       }
-      if (crank == 0) p.lse[(int64_t)t * 128 + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
+      if (crank == 0 && real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
     }
   }
 
@@ -485,7 +490,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   float* xchg = tc_xchg_ptr();
   if (!xchg) return cudaErrorInvalidSymbol;
-  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.topk, a.scale * kLog2e};
+  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.scale * kLog2e};
   tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }

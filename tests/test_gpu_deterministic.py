@@ -5,8 +5,9 @@ right in ascending slot order.  Checked here: the same bits on repeated runs and
 for any chunking of the query tokens (a workspace that fits only a few tokens'
 contributions), dq identical to the atomic mode's, and parity with the oracle
 on the same inputs as the atomic mode.  Cases cover the tensor-core path
-(H = 128, with padding holes), the CUDA-core path with one head group (H = 16)
-and with two head groups whose contributions are added in order (H = 64).
+(H = 16, 64 and 128, with padding holes) and the CUDA-core path (top-k above
+the tensor-core limit) with two head groups whose contributions are added in
+order (H = 64).
 """
 import numpy as np
 import pytest
@@ -25,11 +26,15 @@ CASES = {
     "H64": lambda: W.make_custom(640, 64, 256, [320, 320], seed=42, empty_rows=2),
     "H128": lambda: W.make_custom(520, 128, 320, [8, 200, 312], seed=43, empty_rows=3),
     "H128-holes": lambda: _with_padding_holes(W.make_custom(500, 128, 512, [500], seed=44, empty_rows=2), 44),
+    # top-k above the tensor-core limit: CUDA-core kernels, two head groups added in order
+    "H64-bigtopk": lambda: W.make_custom(150, 64, 16448, [150], seed=45, empty_rows=2),
 }
 
 
 def _contribution_bytes_per_token(w):
-    groups = 1 if (w.H == 128 or w.H <= 16) else w.H // 32
+    # the tensor-core kernels store one contribution per slot; above their top-k limit the
+    # CUDA-core kernels store one per head group of 32 heads (one for H <= 16)
+    groups = 1 if (w.topk <= 16384 or w.H <= 16) else w.H // 32
     return groups * w.topk * 576 * 4
 
 
@@ -85,7 +90,8 @@ def test_deterministic_bits_do_not_depend_on_chunking(case, chunk_tokens):
     _, dkv_full, _ = _bwd(w, d, out_in, lse_in, capi.SMLA_DKV_DETERMINISTIC)
     full = capi.sparse_mla_bwd_workspace_bytes(w.T, w.H, w.topk, capi.SMLA_DKV_DETERMINISTIC)
     per_tok = _contribution_bytes_per_token(w)
-    fixed = full - w.T * per_tok                # every token fits in the default chunk at these sizes
+    default_tokens = min(w.T, max(1, (4 << 30) // per_tok))   # the library's default chunk (4 GiB)
+    fixed = full - default_tokens * per_tok
     ws = torch.empty(fixed + chunk_tokens * per_tok, dtype=torch.uint8, device=d["q"].device)
     _, dkv_small, _ = _bwd(w, d, out_in, lse_in, capi.SMLA_DKV_DETERMINISTIC, workspace=ws)
     assert torch.equal(dkv_small, dkv_full)

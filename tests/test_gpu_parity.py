@@ -43,8 +43,9 @@ SMALL = {
                                               q_std=8.0),
     # whole blocks of padding between valid slots
     "holes-H128": lambda: _with_padding_holes(W.make_custom(600, 128, 512, [600], seed=16, empty_rows=2), 16),
-    # top-k above the tensor-core kernels' limit (runs the CUDA-core kernels at H = 128)
+    # top-k above the tensor-core kernels' limit (runs the CUDA-core kernels)
     "bigtopk-H128": lambda: W.make_custom(260, 128, 16448, [260], seed=17, empty_rows=2),
+    "bigtopk-H8": lambda: W.make_custom(200, 8, 16448, [200], seed=18, empty_rows=2),
 }
 
 
