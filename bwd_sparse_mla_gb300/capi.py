@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_launch_count.restype = ctypes.c_uint64
     lib.sparse_mla_wait_selftest.argtypes = [P]
     lib.sparse_mla_wait_selftest.restype = I
+    lib.sparse_mla_topk.argtypes = [P, ctypes.c_int64, I, I, P, I, I, P, P]
+    lib.sparse_mla_topk.restype = I
     _lib = lib
     return lib
 
@@ -84,6 +86,20 @@ def sparse_mla_wait_selftest(stream=None) -> None:
     up after 1 s and sets the device status word to 1 (read and clear it with
     sparse_mla_device_status(clear=True))."""
     _check(load().sparse_mla_wait_selftest(_stream(stream)))
+
+
+def sparse_mla_topk(scores, cu_seqlens, topk: int, ncols: int | None = None, indices=None, stream=None):
+    """indices [T, 1, topk] int32: per row the best min(topk, causal count) candidates
+    of scores [T, ncols] (fp32, row-major) as packed kv rows, -1 padded."""
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be a row-major [T, ncols] float32 tensor")
+    T = scores.shape[0]
+    ncols = scores.shape[1] if ncols is None else int(ncols)
+    if indices is None:
+        indices = torch.empty((T, 1, topk), dtype=torch.int32, device=scores.device)
+    _check(load().sparse_mla_topk(_ptr(scores), scores.stride(0), T, ncols, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                  int(topk), _ptr(indices), _stream(stream)))
+    return indices
 
 
 def _check(rc: int) -> None:

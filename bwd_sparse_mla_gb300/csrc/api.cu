@@ -74,6 +74,7 @@ int check_shape(int T, int H, int topk, float scale) {
 
 size_t delta_bytes(int T, int H) { return (((size_t)T * H * sizeof(float)) + 255) & ~(size_t)255; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr size_t kTopkSmemLimit = 220 * 1024;   // dynamic shared memory of the top-k selection
 
 // Workspace of the deterministic dKV mode: Delta, the per-row slot lists (CSR:
 // offset, fill cursor, reduction cursor, scan scratch, sorted slot ids) and the
@@ -130,6 +131,30 @@ int sparse_mla_wait_selftest(void* stream) {
   if (int r = check_device()) return r;
   cudaError_t e = smla::launch_wait_selftest(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_wait_selftest launch");
+  count_launches(1);
+  return 0;
+}
+
+int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int32_t* cu_seqlens, int B, int topk,
+                    int32_t* indices, void* stream) {
+  g_last_error.clear();
+  if (T < 0) return fail(-EINVAL, "T must be >= 0 (got %d)", T);
+  if (ncols <= 0 || ld < ncols) return fail(-EINVAL, "need 0 < ncols <= ld (got ncols %d, ld %lld)", ncols, (long long)ld);
+  if (topk <= 0) return fail(-EINVAL, "topk must be positive (got %d)", topk);
+  if (B < 1) return fail(-EINVAL, "B must be >= 1 (got %d)", B);
+  if (smla::topk_smem_bytes(ncols, topk) > kTopkSmemLimit)
+    return fail(-EINVAL, "ncols %d with topk %d exceeds the shared-memory selection (4 ncols + 8 topk rounded up to a "
+                "power of two <= %zu bytes)", ncols, topk, kTopkSmemLimit);
+  if (T == 0) return 0;
+  if (scores == nullptr || cu_seqlens == nullptr || indices == nullptr)
+    return fail(-EINVAL, "scores, cu_seqlens and indices must not be NULL");
+  if (int r = check_device()) return r;
+  int dev = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = smla::launch_topk(scores, ld, ncols, cu_seqlens, B, T, topk, indices, nsm, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_topk launch");
   count_launches(1);
   return 0;
 }

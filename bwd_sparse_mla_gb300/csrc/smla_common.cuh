@@ -98,6 +98,10 @@ cudaError_t launch_reduce_rows(const int* offset, const int* seg, int* pos, cons
                                int64_t gstride, int64_t slot_lo, int64_t slot_hi, int T, float* dkv32,
                                cudaStream_t s);
 int simt_head_groups(int H);   // CUDA-core backward: CTAs (head groups) per token
+// top-k index selection (topk.cu)
+size_t topk_smem_bytes(int ncols, int topk);
+cudaError_t launch_topk(const float* scores, int64_t ld, int ncols, const int32_t* cu, int B, int T, int topk,
+                        int32_t* out, int num_sms, cudaStream_t s);
 cudaError_t launch_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
                                  int B, unsigned long long* counter, cudaStream_t s);
 

@@ -162,6 +162,30 @@ int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const sm
 int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
                              int B, int64_t* n_bad, void* stream);
 
+/*
+ * Top-k index selection that produces `indices` for the calls above
+ * (Megatron-Bridge PR #17, "GLM-5 DSA option: tilelang (2/2)", Summary and Bug
+ * fixes: the indexer's top-k is capped at the keys a query can see in its own
+ * sequence and padded to the fixed width with -1).
+ *   scores   [T, ld] fp32 (device): row t scores its causal candidates, the rows
+ *            s0 .. t of its own sequence, in columns 0 .. t - s0 (s0 = start of
+ *            t's sequence); columns past t - s0 are not read
+ *   ncols    columns that may hold candidates (a longer sequence is capped at
+ *            its first ncols keys); ncols <= ld
+ *   cu_seqlens [B+1] int32 (device): 0 = cu[0] <= cu[1] <= ... <= cu[B] = T
+ *   topk     width of each index row
+ *   indices  [T, 1, topk] int32 (device, written): the k = min(topk, t - s0 + 1,
+ *            ncols) best candidates as packed kv rows s0 + c, in descending
+ *            score order (equal scores by ascending c; NaN scores last),
+ *            then -1
+ * Needs 4 * ncols + 8 * (topk rounded up to a power of two) <= 220 KiB of
+ * shared memory (e.g. ncols 32768 with topk 8192), else -EINVAL.  Asynchronous
+ * on `stream`.  The pages have no kernel for this step beyond the padding rule;
+ * one CTA per row selects by a radix select in shared memory.
+ */
+int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int32_t* cu_seqlens, int B, int topk,
+                    int32_t* indices, void* stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* sparse_mla_last_error(void);
 

@@ -118,3 +118,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         capi.load()
+
+
+def test_topk_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    ok = dict(ld=64, T=16, ncols=64, B=1, topk=8)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.sparse_mla_topk(FAKE, a["ld"], a["T"], a["ncols"], FAKE, a["B"], a["topk"], FAKE, None)
+    assert call(ncols=65) == EINVAL                         # ncols > ld
+    assert call(topk=0) == EINVAL
+    assert call(B=0) == EINVAL
+    assert call(ld=60000, ncols=60000) == EINVAL            # beyond the shared-memory selection
+    assert "shared-memory selection" in capi.sparse_mla_last_error()
+    assert call(T=0) == 0
+    assert lib.sparse_mla_topk(None, 64, 16, 64, FAKE, 1, 8, FAKE, None) == EINVAL
+
