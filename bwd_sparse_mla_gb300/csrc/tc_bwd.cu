@@ -14,11 +14,12 @@
 //              zero bytes: exact-zero K/V rows);
 //   MMA      : S_half = q_half K_half^T and dP_half = dO_half V_half^T
 //              (M=128 heads, N=32 slots) into TMEM;
-//   exchange : one thread per head writes its partial S and dP rows to this
-//              SM's slot of an L2 exchange scratch, reads the peer CTA's rows
-//              from its slot, and stores the sums back into TMEM (both CTAs
-//              obtain bit-identical sums);
-//   softmax  : one thread per head loads the full S and dP rows, recomputes
+//   exchange : one thread per head loads its partial S and dP rows and writes
+//              them to this SM's slot of an L2 exchange scratch;
+//   softmax  : one thread per head loads its own partial rows (the TMEM buffer
+//              is then free for the next block's S / dP), adds the peer CTA's
+//              rows read from the peer's slot (both CTAs obtain bit-identical
+//              sums), recomputes
 //              P = exp2(S*scale*log2e - lse*log2e) (0 on padding slots),
 //              dS' = scale * P * (dP - Delta), and stores P and dS' each as
 //              a bf16 pair hi + lo (x - hi rounded again), so the dQ and dKV
@@ -26,8 +27,8 @@
 //   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
 //              transposed dKV tiles dKV^T[d, j] = dO^T (hi + lo) + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
-//   drain    : the exchange warps (slot columns 0..15) and the softmax warps
-//              (16..31) read the previous block's dKV tiles from TMEM and add
+//   drain    : the exchange warps (slot columns 0..19) and the softmax warps
+//              (20..31) read the previous block's dKV tiles from TMEM and add
 //              them into the fp32 dKV rows named by the valid slots (coalesced
 //              128-byte fp32 reductions; padding slots issue no write, the
 //              no-op the miles PR #2079 summary describes for the clamped atomic).
@@ -67,7 +68,7 @@ constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;         // blocks with a valid s
 constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;        // their number
 constexpr int SM_BAR = SM_NB + 8;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 9,
-           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, S_SUM = 15, NBAR = 16 };
+           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, NBAR = 15 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 8;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -98,24 +99,24 @@ struct TcBwdParams {
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
 
-// Adds half `half` (16 of the 32 slot columns) of block j's dKV^T tiles into the
-// fp32 rows the valid slots name.  `rows`: lane k holds the row of slot k (-1 for
+// Adds slot columns [C0, C0 + NC) of block j's dKV^T tiles into the fp32 rows
+// the valid slots name.  `rows`: lane k holds the row of slot k (-1 for
 // padding).  Dims of tile m: CTA 0 -> [0,128), [128,256), tail [512,576);
 // CTA 1 -> [256,384), [384,512).  Called by a full set of four warps (one per
-// TMEM lane quarter); each thread arrives once per block on the DKV_FREE barrier.
-// With kStore (deterministic mode) the slot rows are stored at gslot + k * 576
+// TMEM lane quarter); each thread arrives once per block on DKV_FREE.  With
+// kStore (deterministic mode) the slot rows are stored at gslot + k * 576
 // (k = slot within the block) instead of added into dkv32.
-template <bool kStore>
-__device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int half,
-                                           int ntile, uint32_t crank, int L, float* dkv32, float* gslot,
-                                           volatile int* abort_flag, uint32_t* status) {
+template <int C0, int NC, bool kStore>
+__device__ __forceinline__ bool drain_cols(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
+                                           uint32_t crank, int L, float* dkv32, float* gslot, volatile int* abort_flag,
+                                           uint32_t* status) {
   if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, status))) return false;
   tc_fence_after();
 #pragma unroll 1
   for (int m = 0; m < ntile; ++m) {
-    float gh[16], gl[16];
-    tmem_ld16(tl + tm_dkv + 64 * m + 16 * half, gh);        // hi half of the slots' columns
-    tmem_ld16(tl + tm_dkv + 64 * m + 32 + 16 * half, gl);   // lo half
+    float gh[NC], gl[NC];
+    tmem_ld_cols<NC>(tl + tm_dkv + 64 * m + C0, gh);        // hi half of the slots' columns
+    tmem_ld_cols<NC>(tl + tm_dkv + 64 * m + 32 + C0, gl);   // lo half
     if (m == ntile - 1) {               // this set's part of every tile is read: the MMA may overwrite them
       tc_fence_before();
       mbar_arrive(bar_addr(sb, DKV_FREE));
@@ -123,11 +124,11 @@ __device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm
     const int d = (crank == 0 ? (m < 2 ? 128 * m : 512) : 256 + 128 * m) + L;
     if (d < kDqk) {                     // warp-uniform: only CTA 0's tail tile has lanes past 576
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int row = __shfl_sync(0xffffffffu, rows, 16 * half + k);
+      for (int k = 0; k < NC; ++k) {
+        const int row = __shfl_sync(0xffffffffu, rows, C0 + k);
         if (row < 0) continue;
         if (kStore)
-          gslot[(16 * half + k) * kDqk + d] = gh[k] + gl[k];
+          gslot[(C0 + k) * kDqk + d] = gh[k] + gl[k];
         else
           red_add_f32(dkv32 + (int64_t)row * kDqk + d, gh[k] + gl[k]);
       }
@@ -136,13 +137,18 @@ __device__ __forceinline__ bool drain_half(uint32_t sb, uint32_t tl, uint32_t tm
   return true;
 }
 
-__device__ __forceinline__ bool drain_half_any(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int half,
-                                               int ntile, uint32_t crank, int L, float* dkv32, float* gslot,
-                                               volatile int* abort_flag, uint32_t* status) {
+template <int C0, int NC>
+__device__ __forceinline__ bool drain_any(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
+                                          uint32_t crank, int L, float* dkv32, float* gslot, volatile int* abort_flag,
+                                          uint32_t* status) {
   return gslot != nullptr
-             ? drain_half<true>(sb, tl, tm_dkv, j, rows, half, ntile, crank, L, dkv32, gslot, abort_flag, status)
-             : drain_half<false>(sb, tl, tm_dkv, j, rows, half, ntile, crank, L, dkv32, gslot, abort_flag, status);
+             ? drain_cols<C0, NC, true>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status)
+             : drain_cols<C0, NC, false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status);
 }
+
+// slot columns of each block drained by the exchange warps ([0, kXchgCols)) and by
+// the softmax warps (the rest): the exchange warps' other work per block is lighter
+constexpr int kXchgCols = 20;
 
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -172,16 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 256);
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
-    mbar_init(bar_addr(sb, SDP_FREE), 128);
-    mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
+    mbar_init(bar_addr(sb, SDP_FREE), 256);      // both warp sets loaded the partial S / dP
+    mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's exchange warps wrote their partial rows
     mbar_init(bar_addr(sb, X_FULL + 1), 128);
-    mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
+    mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's softmax warps read ours
     mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
     mbar_init(bar_addr(sb, DKV_FREE), 256);      // both warp sets loaded their half of the tiles
-    mbar_init(bar_addr(sb, S_SUM), 128);        // full S / dP stored back into TMEM
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -375,17 +380,33 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     uint8_t* prow = smem + SM_P + h * 128;
     uint8_t* dsrow = smem + SM_DS + h * 128;
     const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
+    // the peer CTA's exchange slot (its partial S / dP rows) and its X_EMPTY barriers
+    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
+    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
+    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     bool ok = true;
     int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
-      const int st = i & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_SUM), i & 1, abort_flag, p.status)))) break;
+      const int st = i & 1, xb = i & 1;
+      // own partial rows; the TMEM buffer is free once both warp sets hold them
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[32], dp[32];
-      tmem_ld32(tl + TM_S, s);          // full rows (own + peer partials)
+      tmem_ld32(tl + TM_S, s);
       tmem_ld32(tl + TM_DP, dp);
       tc_fence_before();
       mbar_arrive(bar_addr(sb, SDP_FREE));
+      // add the peer's partial rows (published by its exchange warps)
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
+        break;
+      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
+        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
+      }
+      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
       const int rows = reinterpret_cast<const int*>(smem + SM_ROWS)[st * 32 + lane];
@@ -417,14 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
-      // second half of the previous block's dKV tiles (the exchange warps drain the first)
-      if (i >= 1 && !(ok = drain_half_any(sb, tl, TM_DKV, i - 1, prev_rows, 1, ntile, crank, h, p.dkv32, gslot(i - 1),
-                                      abort_flag, p.status)))
+      // the softmax warps' columns of the previous block's dKV tiles
+      if (i >= 1 && !(ok = drain_any<kXchgCols, kBK - kXchgCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, h,
+                                                                 p.dkv32, gslot(i - 1), abort_flag, p.status)))
         break;
       prev_rows = rows;
     }
     if (ok && nb > 0)
-      ok = drain_half_any(sb, tl, TM_DKV, nb - 1, prev_rows, 1, ntile, crank, h, p.dkv32, gslot(nb - 1), abort_flag, p.status);
+      ok = drain_any<kXchgCols, kBK - kXchgCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, h, p.dkv32,
+                                                 gslot(nb - 1), abort_flag, p.status);
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
@@ -450,27 +472,30 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     }
   } else {
     // ------------------------------------------------------------ exchange + dKV drain
+    // Publishes this CTA's partial S / dP rows of each block to its L2 exchange
+    // slot (the peer's softmax warps read them), then drains the first half of
+    // the previous block's dKV tiles.
     const int q4 = warp & 3;
     const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
-    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
     const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
     float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + L;
-    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + L;
 
     bool ok = true;
     int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
-      // exchange block i: partial S / dP rows through L2, buffer i&1 of the SM slots
+      // partial S / dP rows of block i into buffer i & 1 of this SM's slot
       const int xb = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
       tc_fence_after();
       float s[32], dp[32];
       tmem_ld32(tl + TM_S, s);
       tmem_ld32(tl + TM_DP, dp);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sb, SDP_FREE));
+      // the peer's softmax warps read this buffer two blocks ago
       if (i >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + xb), ((i >> 1) - 1) & 1,
                                                                    abort_flag, p.status))))
         break;
@@ -481,34 +506,20 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
       }
       mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
-        break;
-      const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
-        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
-        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
-      }
-      mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
-      tmem_st32(tl + TM_S, s);
-      tmem_st32(tl + TM_DP, dp);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, S_SUM));
-      // row list of block i (the softmax warps read it too), then the first half of
-      // the previous block's dKV tiles
+      // row list of block i (the softmax warps read it too), then the exchange
+      // warps' columns of the previous block's dKV tiles
       const int st = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const int rows = srows[st * 32 + lane];
       mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      if (i >= 1 && !(ok = drain_half_any(sb, tl, TM_DKV, i - 1, prev_rows, 0, ntile, crank, L, p.dkv32, gslot(i - 1),
-                                      abort_flag, p.status)))
+      if (i >= 1 && !(ok = drain_any<0, kXchgCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, L, p.dkv32,
+                                                   gslot(i - 1), abort_flag, p.status)))
         break;
       prev_rows = rows;
     }
     if (ok && nb > 0)
-      drain_half_any(sb, tl, TM_DKV, nb - 1, prev_rows, 0, ntile, crank, L, p.dkv32, gslot(nb - 1), abort_flag, p.status);
+      drain_any<0, kXchgCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, L, p.dkv32, gslot(nb - 1), abort_flag,
+                              p.status);
   }
 
   // ------------------------------------------------------------ teardown

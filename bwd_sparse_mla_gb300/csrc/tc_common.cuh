@@ -285,6 +285,24 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const float* v) {
       : "memory");
 }
 // 32 lanes x 32 bits, 32 consecutive columns per thread (load + wait).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(taddr)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
@@ -296,6 +314,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
       : "r"(taddr)
       : "memory");
 }
+
+// NC consecutive 32-bit columns (NC a multiple of 4, up to 28) from taddr
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
+  static_assert(NC % 4 == 0 && NC <= 28, "columns");
+  if constexpr (NC >= 16) {
+    tmem_ld16(taddr, v);
+    if constexpr (NC > 16) tmem_ld_cols<NC - 16>(taddr + 16, v + 16);
+  } else if constexpr (NC >= 8) {
+    tmem_ld8(taddr, v);
+    if constexpr (NC > 8) tmem_ld_cols<NC - 8>(taddr + 8, v + 8);
+  } else if constexpr (NC == 4) {
+    tmem_ld4(taddr, v);
+  }
+}
+
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
