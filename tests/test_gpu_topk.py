@@ -30,6 +30,10 @@ def _scores(seed, T, ncols, tie_levels=None, nan_frac=0.0):
     (900, 256, 64, [1, 2, 400, 497], 8, 0.0),       # sequences longer than ncols are capped
     (4096, 4096, 2048, [4096], None, 0.0),          # headline-like width
     (513, 512, 8192, [513], 2, 0.01),               # topk wider than any candidate list
+    (3000, 3000, 4096, [3000], None, 0.0),          # k up to 3000: four sorted pairs a thread
+    (6000, 6000, 8192, [1000, 5000], 4, 0.01),      # k up to 5000: eight sorted pairs a thread
+    (4096, 4096, 1024, [4096], 1, 0.01),            # ties at the threshold overflow the buffer: ordered collect
+    (3000, 3000, 2048, [3000], 1e-9, 0.0),          # every score 0 or -0: all tie, columns in order
 ])
 def test_topk_matches_oracle(T, ncols, topk, lens, ties, nan, cuda_device):
     s = _scores(7 + T + topk, T, ncols, ties, nan)
