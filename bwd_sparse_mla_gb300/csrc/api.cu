@@ -140,11 +140,11 @@ int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int
   g_last_error.clear();
   if (T < 0) return fail(-EINVAL, "T must be >= 0 (got %d)", T);
   if (ncols <= 0 || ld < ncols) return fail(-EINVAL, "need 0 < ncols <= ld (got ncols %d, ld %lld)", ncols, (long long)ld);
-  if (topk <= 0) return fail(-EINVAL, "topk must be positive (got %d)", topk);
+  if (topk <= 0 || topk > 8192) return fail(-EINVAL, "topk must be in [1, 8192] (got %d)", topk);
   if (B < 1) return fail(-EINVAL, "B must be >= 1 (got %d)", B);
   if (smla::topk_smem_bytes(ncols, topk) > kTopkSmemLimit)
-    return fail(-EINVAL, "ncols %d with topk %d exceeds the shared-memory selection (4 ncols + 8 topk rounded up to a "
-                "power of two <= %zu bytes)", ncols, topk, kTopkSmemLimit);
+    return fail(-EINVAL, "ncols %d with topk %d exceeds the shared-memory selection (4 (ncols + 3) + 8 max(1024, topk "
+                "rounded up to a power of two) <= %zu bytes)", ncols, topk, kTopkSmemLimit);
   if (T == 0) return 0;
   if (scores == nullptr || cu_seqlens == nullptr || indices == nullptr)
     return fail(-EINVAL, "scores, cu_seqlens and indices must not be NULL");

@@ -9,7 +9,8 @@
 // One CTA per row: the row's scores are mapped to order-preserving 32-bit keys
 // in shared memory; a 4-pass radix select (8 bits per pass, the first fused
 // with the load, the bin chosen by a warp-parallel suffix scan) finds the k-th
-// largest key thr.  When every key >= thr fits in the selection buffer they
+// largest key thr (stopping early once the boundary bin is taken whole).
+// When every key >= thr fits in the selection buffer they
 // are collected in one pass in any order; otherwise (many ties at thr) an
 // ordered pass collects the keys above thr and the first columns equal to it.
 // A bitonic network unrolled at compile time, held in registers (shuffles
@@ -20,6 +21,7 @@ namespace smla {
 namespace {
 
 constexpr int kTkThreads = 1024;
+constexpr int kTkCuCache = 1024;          // sequences whose starts are kept in shared memory
 
 // larger float -> larger key; -0 and +0 equal; NaN below everything
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -121,22 +123,29 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
                                                           int kpow2, int32_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t sm[];
   unsigned long long* sel = reinterpret_cast<unsigned long long*>(sm);   // kpow2 selected (key, column)
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + kpow2);             // ncols keys
+  uint32_t* keys_base = reinterpret_cast<uint32_t*>(sel + kpow2);        // ncols + 3 keys
   __shared__ int hist[2][256];           // radix histograms, alternating between passes
+  __shared__ int cu_s[kTkCuCache + 1];
   __shared__ int warp_cnt[32];
   __shared__ int info[5];                 // s0, chosen bin, remaining, chunk total, keys equal to the bin
   __shared__ int n_sel, n_eq;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int32_t* cus = cu;
+  if (B <= kTkCuCache) {
+    for (int i = tid; i <= B; i += kTkThreads) cu_s[i] = cu[i];
+    cus = cu_s;
+  }
+  __syncthreads();
 
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     if (tid == 0) {                       // start of t's sequence: largest b with cu[b] <= t
       int lo = 0, hi = B;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+        if (cus[mid] <= t) lo = mid; else hi = mid - 1;
       }
-      info[0] = cu[lo];
+      info[0] = cus[lo];
       n_sel = 0;
       n_eq = 0;
     }
@@ -146,12 +155,30 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
     const int n = min(t - s0 + 1, ncols);
     const int k = min(topk, n);
     const float* row = scores + (int64_t)t * ld;
-    // keys, with the histogram of their top byte (the first radix pass)
-#pragma unroll 4
-    for (int c = tid; c < n; c += kTkThreads) {
-      const uint32_t kk = order_key(row[c]);
-      keys[c] = kk;
-      atomicAdd(&hist[0][kk >> 24], 1);
+    // keys, with the histogram of their top byte (the first radix pass).
+    // Columns [0, head) and the tail are read singly, the rest as aligned
+    // float4; keys is offset so that keys + head is 16-byte aligned too.
+    const int head = min((int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2), n);
+    const int nv = (n - head) >> 2;
+    uint32_t* keys = keys_base + ((4 - head) & 3);
+#pragma unroll 2
+    for (int q = tid; q < nv; q += kTkThreads) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(row + head) + q);
+      const uint4 kk = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+      reinterpret_cast<uint4*>(keys + head)[q] = kk;
+      atomicAdd(&hist[0][kk.x >> 24], 1);
+      atomicAdd(&hist[0][kk.y >> 24], 1);
+      atomicAdd(&hist[0][kk.z >> 24], 1);
+      atomicAdd(&hist[0][kk.w >> 24], 1);
+    }
+    {
+      const int rest = n - head - 4 * nv;           // at most 3 at the tail
+      const int c = tid < head ? tid : head + 4 * nv + (tid - head);
+      if (tid < head + rest) {
+        const uint32_t kk = order_key(row[c]);
+        keys[c] = kk;
+        atomicAdd(&hist[0][kk >> 24], 1);
+      }
     }
     for (int i = tid; i < kpow2; i += kTkThreads) sel[i] = 0ull;   // padding sorts last
     if (tid < 256) hist[1][tid] = 0;
@@ -164,6 +191,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
     for (int p = 0; p < 4; ++p) {
       const int shift = 24 - 8 * p;
       if (p > 0) {
+#pragma unroll 4
         for (int c = tid; c < n; c += kTkThreads) {
           const uint32_t kk = keys[c];
           if ((kk & mask) == prefix) atomicAdd(&hist[p & 1][(kk >> shift) & 255u], 1);
@@ -207,6 +235,9 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
       mask |= 0xffu << shift;
       remaining = info[2];
       eq_total = info[4];
+      // the chosen bin is taken whole: the keys >= prefix (lower bits zero)
+      // are exactly the k wanted
+      if (remaining == eq_total) break;
     }
     const uint32_t thr = prefix;
 
@@ -215,15 +246,25 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
       // every key >= thr fits: collect them in any order; sorting by (key,
       // column) then puts the k wanted first
       nsort = k - remaining + eq_total;
-      for (int base = 0; base < n; base += kTkThreads) {
-        const int c = base + tid;
-        const uint32_t kk = c < n ? keys[c] : 0u;
-        const bool take = c < n && kk >= thr;
-        const unsigned ball = __ballot_sync(0xffffffffu, take);
+      for (int base = 0; base < n; base += 4 * kTkThreads) {
+        uint32_t kk[4];
+        unsigned ball[4];
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = base + u * kTkThreads + tid;
+          kk[u] = c < n ? keys[c] : 0u;
+          ball[u] = __ballot_sync(0xffffffffu, c < n && kk[u] >= thr);
+          cnt += __popc(ball[u]);
+        }
         int pos = 0;
-        if (lane == 0 && ball) pos = atomicAdd(&n_sel, __popc(ball));
-        pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(ball & lt_mask);
-        if (take) sel[pos] = sel_entry(kk, c);
+        if (lane == 0 && cnt) pos = atomicAdd(&n_sel, cnt);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if ((ball[u] >> lane) & 1u) sel[pos + __popc(ball[u] & lt_mask)] = sel_entry(kk[u], base + u * kTkThreads + tid);
+          pos += __popc(ball[u]);
+        }
       }
       __syncthreads();
     } else {
@@ -273,14 +314,17 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float* __restric
 
 }  // namespace
 
-// the selection buffer holds max(next power of two above topk, 1024) pairs
+// the selection buffer holds max(next power of two above topk, 1024) pairs;
+// the keys (ncols, shifted by up to 3 for alignment) follow it
 int topk_sel_entries(int topk) {
   int kp = kTkThreads;
   while (kp < topk) kp <<= 1;
   return kp;
 }
 
-size_t topk_smem_bytes(int ncols, int topk) { return (size_t)topk_sel_entries(topk) * 8 + (size_t)ncols * 4; }
+size_t topk_smem_bytes(int ncols, int topk) {
+  return (size_t)topk_sel_entries(topk) * 8 + (((size_t)ncols + 3) * 4 + 15) / 16 * 16;
+}
 
 cudaError_t launch_topk(const float* scores, int64_t ld, int ncols, const int32_t* cu, int B, int T, int topk,
                         int32_t* out, int num_sms, cudaStream_t s) {

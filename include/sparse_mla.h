@@ -173,15 +173,16 @@ int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int3
  *   ncols    columns that may hold candidates (a longer sequence is capped at
  *            its first ncols keys); ncols <= ld
  *   cu_seqlens [B+1] int32 (device): 0 = cu[0] <= cu[1] <= ... <= cu[B] = T
- *   topk     width of each index row
+ *   topk     width of each index row, 1 .. 8192
  *   indices  [T, 1, topk] int32 (device, written): the k = min(topk, t - s0 + 1,
  *            ncols) best candidates as packed kv rows s0 + c, in descending
  *            score order (equal scores by ascending c; NaN scores last),
  *            then -1
- * Needs 4 * ncols + 8 * (topk rounded up to a power of two) <= 220 KiB of
- * shared memory (e.g. ncols 32768 with topk 8192), else -EINVAL.  Asynchronous
- * on `stream`.  The pages have no kernel for this step beyond the padding rule;
- * one CTA per row selects by a radix select in shared memory.
+ * Needs 4 * (ncols + 3) + 8 * max(1024, topk rounded up to a power of two)
+ * <= 220 KiB of shared memory (e.g. ncols 32768 with topk 8192), else -EINVAL.
+ * Asynchronous on `stream`.  The pages have no kernel for this step beyond the
+ * padding rule; one CTA per row selects by a radix select in shared memory and
+ * sorts the selection with a bitonic network.
  */
 int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int32_t* cu_seqlens, int B, int topk,
                     int32_t* indices, void* stream);

@@ -129,6 +129,8 @@ def test_topk_rejects_bad_arguments(lib):
         return lib.sparse_mla_topk(FAKE, a["ld"], a["T"], a["ncols"], FAKE, a["B"], a["topk"], FAKE, None)
     assert call(ncols=65) == EINVAL                         # ncols > ld
     assert call(topk=0) == EINVAL
+    assert call(topk=8193, ncols=64) == EINVAL           # the sort holds 8 pairs per thread of 1024
+    assert "topk" in capi.sparse_mla_last_error()
     assert call(B=0) == EINVAL
     assert call(ld=60000, ncols=60000) == EINVAL            # beyond the shared-memory selection
     assert "shared-memory selection" in capi.sparse_mla_last_error()
