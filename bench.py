@@ -384,13 +384,16 @@ def traffic_record():
         return None
 
 
+# sources of the backward kernel whose DRAM traffic the record holds
+TRAFFIC_SOURCES = ("tc_bwd.cu", "tc_common.cuh", "smla_common.cuh")
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bwd_sparse_mla_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in TRAFFIC_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
