@@ -330,6 +330,7 @@ def run_ours(args):
     e2e = None
     if rank == 0 or world > 1:
         e2e = run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu)
+        e2e["matches_device_step"] = same_results(e2e.pop("_host"), (out, lse, dq, dkv), dev)
         if world > 1:
             t = torch.tensor([e2e["ms_per_step"]], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -397,11 +398,36 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+E2E_CHUNKS = 16
+
+
+def same_results(host, device, dev, rows=4096):
+    """The streamed step's host results against the device-resident step's (same
+    inputs): out, lse and dq bit for bit; dkv, the bf16 of an fp32 sum taken in
+    another order, within one bf16 step.  Compared in slices of rows."""
+    import torch
+    ok = True
+    for i, (h, d) in enumerate(zip(host, device)):
+        for r0 in range(0, d.shape[0], rows):
+            a, b = h[r0:r0 + rows].to(dev), d[r0:r0 + rows]
+            if i < 3:
+                ok &= bool(torch.equal(a, b))
+            else:
+                a, b = a.float(), b.float()
+                floor = 1e-5 * float(b.abs().max()) + 1e-30      # sums that cancel to near zero
+                ok &= bool(((a - b).abs() <= b.abs() * 2.0 ** -7 + floor).all())
+    return ok
+
+
 def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     """Same step through the public API from pinned host buffers: H2D of the
     inputs, forward, backward, D2H of out, lse, dq and dkv (bf16), all inside the
-    timed region.  The copies run on their own streams: dO is uploaded while the
-    forward runs, and out / lse are downloaded while the backward runs."""
+    timed region.  The step streams through the device in E2E_CHUNKS ranges of
+    query rows (sparse_mla_fwd_rows / sparse_mla_bwd_rows / sparse_mla_dkv_cast):
+    the forward of a range starts as soon as its q and indices have landed, dO
+    uploads while the forward runs, each range's out / lse and dq download while
+    later ranges compute, and dkv (fp32, accumulated over all ranges) is cast
+    and downloaded last.  Copies run on their own streams."""
     import torch
     T, H, topk = w.T, w.H, w.topk
     pin = lambda t: t.pin_memory()  # noqa: E731
@@ -420,36 +446,52 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     d_dq = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
     d_dkv32 = torch.empty((T, 1, 576), dtype=torch.float32, device=dev)
     d_dkv = torch.empty((T, 1, 576), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk, args.dkv_mode), 256), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk), 256), dtype=torch.uint8, device=dev)
     cs = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bounds = [round(i * T / E2E_CHUNKS) for i in range(E2E_CHUNKS + 1)]
+    ranges = [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(E2E_CHUNKS) if bounds[i + 1] > bounds[i]]
 
     def one(start):
-        ev = {k: torch.cuda.Event() for k in ("in1", "in2", "fwd", "bwd", "done")}
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        ev_meta, ev_cast, ev_done = ev(), ev(), ev()
+        ev_q, ev_do, ev_f, ev_b = ([ev() for _ in ranges] for _ in range(4))
         s_in.wait_event(start)
         with torch.cuda.stream(s_in):
-            for d, h in ((d_q, hq), (d_kv, hkv), (d_idx, hidx), (d_cu, hcu)):
-                d.copy_(h, non_blocking=True)
-            ev["in1"].record(s_in)
-            d_do.copy_(hdo, non_blocking=True)            # overlaps the forward
-            ev["in2"].record(s_in)
-        cs.wait_event(ev["in1"])
-        capi.sparse_mla_fwd(d_q, d_kv, d_idx, d_cu, w.scale, out=d_out, lse=d_lse)
-        ev["fwd"].record(cs)
-        cs.wait_event(ev["in2"])
-        capi.sparse_mla_bwd(d_q, d_kv, d_out, d_do, d_lse, d_idx, d_cu, w.scale, dkv_mode=args.dkv_mode, dq=d_dq,
-                            dkv_f32=d_dkv32, dkv=d_dkv, workspace=ws)
-        ev["bwd"].record(cs)
-        s_out.wait_event(ev["fwd"])
+            d_kv.copy_(hkv, non_blocking=True)
+            d_cu.copy_(hcu, non_blocking=True)
+            ev_meta.record(s_in)
+            for c, (t0, nt) in enumerate(ranges):
+                d_q[t0:t0 + nt].copy_(hq[t0:t0 + nt], non_blocking=True)
+                d_idx[t0:t0 + nt].copy_(hidx[t0:t0 + nt], non_blocking=True)
+                ev_q[c].record(s_in)
+            for c, (t0, nt) in enumerate(ranges):       # overlaps the forward
+                d_do[t0:t0 + nt].copy_(hdo[t0:t0 + nt], non_blocking=True)
+                ev_do[c].record(s_in)
+        cs.wait_event(ev_meta)
+        d_dkv32.zero_()                                # the row-range backward adds into it
+        for c, (t0, nt) in enumerate(ranges):
+            cs.wait_event(ev_q[c])
+            capi.sparse_mla_fwd_rows(d_q, d_kv, d_idx, d_cu, w.scale, t0, nt, d_out, d_lse)
+            ev_f[c].record(cs)
+        for c, (t0, nt) in enumerate(ranges):
+            cs.wait_event(ev_do[c])
+            capi.sparse_mla_bwd_rows(d_q, d_kv, d_out, d_do, d_lse, d_idx, d_cu, w.scale, t0, nt, d_dq, d_dkv32, ws)
+            ev_b[c].record(cs)
+        capi.sparse_mla_dkv_cast(d_dkv32, d_dkv)
+        ev_cast.record(cs)
         with torch.cuda.stream(s_out):
-            o_out.copy_(d_out, non_blocking=True)         # overlaps the backward
-            o_lse.copy_(d_lse, non_blocking=True)
-            s_out.wait_event(ev["bwd"])
-            o_dq.copy_(d_dq, non_blocking=True)
+            for c, (t0, nt) in enumerate(ranges):
+                s_out.wait_event(ev_f[c])
+                o_out[t0:t0 + nt].copy_(d_out[t0:t0 + nt], non_blocking=True)
+                o_lse[t0:t0 + nt].copy_(d_lse[t0:t0 + nt], non_blocking=True)
+            for c, (t0, nt) in enumerate(ranges):
+                s_out.wait_event(ev_b[c])
+                o_dq[t0:t0 + nt].copy_(d_dq[t0:t0 + nt], non_blocking=True)
+            s_out.wait_event(ev_cast)
             o_dkv.copy_(d_dkv, non_blocking=True)
-            ev["done"].record(s_out)
-        cs.wait_event(ev["done"])
+            ev_done.record(s_out)
+        cs.wait_event(ev_done)
 
     warm = torch.cuda.Event()
     warm.record(cs)
@@ -465,9 +507,14 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     ms = float(np.mean(times))
+    # the streamed step's results against the device-resident step (same inputs): out, lse and dq bit
+    # for bit, dkv (bf16 of an fp32 sum in another order) within one bf16 step
     return {"value": T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": steps,
-            "overlap": "dO upload during the forward, out / lse download during the backward (separate streams)"}
+            "ms_per_step": ms, "steps": steps, "chunks": len(ranges), "dkv_mode": "atomic",
+            "overlap": f"streamed in {len(ranges)} ranges of query rows: q / indices upload overlaps the forward "
+                       "of earlier ranges, dO upload the forward, out / lse and dq download later ranges' work "
+                       "(separate copy streams)",
+            "_host": (o_out, o_lse, o_dq, o_dkv)}
 
 
 def main():

@@ -39,6 +39,12 @@ def load() -> ctypes.CDLL:
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.sparse_mla_fwd.argtypes = [P, P, P, P, I, I, I, I, F, P, P, P]
     lib.sparse_mla_fwd.restype = I
+    lib.sparse_mla_fwd_rows.argtypes = [P, P, P, P, I, I, I, I, F, I, I, P, P, P]
+    lib.sparse_mla_fwd_rows.restype = I
+    lib.sparse_mla_bwd_rows.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, I, P, P, P, S, P]
+    lib.sparse_mla_bwd_rows.restype = I
+    lib.sparse_mla_dkv_cast.argtypes = [P, P, I, P]
+    lib.sparse_mla_dkv_cast.restype = I
     lib.sparse_mla_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.sparse_mla_bwd_workspace_bytes.restype = S
     lib.sparse_mla_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, P, P, P, P, S, P]
@@ -136,6 +142,34 @@ def sparse_mla_fwd(q, kv, indices, cu_seqlens, scale, out=None, lse=None, stream
     _check(load().sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(cu_seqlens), T, H, topk, B,
                                  float(scale), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def sparse_mla_fwd_rows(q, kv, indices, cu_seqlens, scale, t0: int, nt: int, out, lse, stream=None):
+    """Forward of query rows [t0, t0 + nt) into the full out [T,H,512] / lse [T,H]
+    (the other rows are neither read nor written)."""
+    T, H, topk = _dims(q, indices)
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(load().sparse_mla_fwd_rows(_ptr(q), _ptr(kv), _ptr(indices), _ptr(cu_seqlens), T, H, topk, B,
+                                      float(scale), int(t0), int(nt), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def sparse_mla_bwd_rows(q, kv, out, dout, lse, indices, cu_seqlens, scale, t0: int, nt: int, dq, dkv_f32,
+                        workspace, stream=None):
+    """Backward of query rows [t0, t0 + nt): writes those rows of dq and ADDS their
+    dKV contributions into dkv_f32 (zeroed by the caller before the first range)."""
+    T, H, topk = _dims(q, indices)
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(load().sparse_mla_bwd_rows(_ptr(q), _ptr(kv), _ptr(out), _ptr(dout), _ptr(lse), _ptr(indices),
+                                      _ptr(cu_seqlens), T, H, topk, B, float(scale), int(t0), int(nt), _ptr(dq),
+                                      _ptr(dkv_f32), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dkv_f32
+
+
+def sparse_mla_dkv_cast(dkv_f32, dkv, stream=None):
+    """dkv (bf16) = round-to-nearest-even of dkv_f32 [T,1,576]."""
+    _check(load().sparse_mla_dkv_cast(_ptr(dkv_f32), _ptr(dkv), dkv_f32.shape[0], _stream(stream)))
+    return dkv
 
 
 def sparse_mla_bwd_workspace_bytes(T: int, H: int, topk: int, dkv_mode: int = SMLA_DKV_ATOMIC) -> int:

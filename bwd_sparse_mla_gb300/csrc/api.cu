@@ -159,14 +159,20 @@ int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int
   return 0;
 }
 
-int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
-                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
-                   smla_bf16_t* out, float* lse, void* stream) {
-  (void)cu_seqlens;
-  (void)B;
-  g_last_error.clear();
-  if (int r = check_shape(T, H, topk, scale)) return r;
-  if (T == 0) return 0;
+}  // extern "C"
+
+namespace {
+
+int check_rows(int T, int t0, int nt) {
+  if (t0 < 0 || nt < 0 || (int64_t)t0 + nt > T)
+    return fail(-EINVAL, "need 0 <= t0, 0 <= nt and t0 + nt <= T (got t0 %d, nt %d, T %d)", t0, nt, T);
+  return 0;
+}
+
+// forward over query rows [t0, t0 + nt); shapes and the range are checked
+int fwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices, int T, int H, int topk,
+             float scale, int t0, int nt, smla_bf16_t* out, float* lse, void* stream) {
+  if (nt == 0) return 0;
   SMLA_REQUIRE_PTR(q);
   SMLA_REQUIRE_PTR(kv);
   SMLA_REQUIRE_PTR(indices);
@@ -174,9 +180,87 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
   SMLA_REQUIRE_PTR(lse);
   if (int r = check_device()) return r;
   smla::FwdArgs a{q, kv, indices, out, lse, T, H, topk, scale};
+  a.t0 = t0;
+  a.nt = nt;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = use_tc(H, topk) ? smla::launch_fwd_tc(a, s) : smla::launch_fwd_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_fwd launch");
+  count_launches(1);
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
+                   const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
+                   smla_bf16_t* out, float* lse, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  return fwd_rows(q, kv, indices, T, H, topk, scale, 0, T, out, lse, stream);
+}
+
+int sparse_mla_fwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
+                        const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale, int t0, int nt,
+                        smla_bf16_t* out, float* lse, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  if (int r = check_rows(T, t0, nt)) return r;
+  return fwd_rows(q, kv, indices, T, H, topk, scale, t0, nt, out, lse, stream);
+}
+
+int sparse_mla_bwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                        const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                        const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale, int t0, int nt,
+                        smla_bf16_t* dq, float* dkv_f32, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)cu_seqlens;
+  (void)B;
+  g_last_error.clear();
+  if (int r = check_shape(T, H, topk, scale)) return r;
+  if (int r = check_rows(T, t0, nt)) return r;
+  if (nt == 0) return 0;
+  SMLA_REQUIRE_PTR(q);
+  SMLA_REQUIRE_PTR(kv);
+  SMLA_REQUIRE_PTR(out);
+  SMLA_REQUIRE_PTR(dout);
+  SMLA_REQUIRE_PTR(lse);
+  SMLA_REQUIRE_PTR(indices);
+  SMLA_REQUIRE_PTR(dq);
+  SMLA_REQUIRE_PTR(dkv_f32);
+  SMLA_REQUIRE_PTR(workspace);
+  if (workspace_bytes < delta_bytes(T, H))
+    return fail(-EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, delta_bytes(T, H));
+  if (int r = check_device()) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Delta of rows t0.. at their own place, so that ranges on other streams never share it
+  float* delta = static_cast<float*>(workspace);
+  const int64_t r0 = (int64_t)t0 * H;
+  cudaError_t e = smla::launch_delta(out + r0 * smla::kDv, dout + r0 * smla::kDv, delta + r0, (int64_t)nt * H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "delta launch");
+  count_launches(1);
+  smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
+  a.t0 = t0;
+  a.nt = nt;
+  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd_rows launch");
+  count_launches(1);
+  return 0;
+}
+
+int sparse_mla_dkv_cast(const float* dkv_f32, smla_bf16_t* dkv, int T, void* stream) {
+  g_last_error.clear();
+  if (T < 0) return fail(-EINVAL, "T must be >= 0 (got %d)", T);
+  if (T == 0) return 0;
+  SMLA_REQUIRE_PTR(dkv_f32);
+  SMLA_REQUIRE_PTR(dkv);
+  if (int r = check_device()) return r;
+  cudaError_t e = smla::launch_cast_bf16(dkv_f32, dkv, (int64_t)T * smla::kDqk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dkv cast launch");
   count_launches(1);
   return 0;
 }

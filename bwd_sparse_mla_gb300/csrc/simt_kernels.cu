@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kNT, 1) fwd_simt_kernel(FwdArgs a) {
   float* s_l = s_m + HG;                           // [HG]
   int* s_row = reinterpret_cast<int*>(s_l + HG);   // [kBK]
 
-  const int t = blockIdx.x;
+  const int t = a.t0 + blockIdx.x;
   const int h0 = blockIdx.y * HG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float c2 = a.scale * kLog2e;
@@ -373,7 +373,9 @@ cudaError_t fwd_launch(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fwd_simt_kernel<HG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  fwd_simt_kernel<HG><<<dim3(a.T, a.H / HG), kNT, sm, s>>>(a);
+  const int nt = a.nt < 0 ? a.T : a.nt;
+  if (nt == 0) return cudaSuccess;
+  fwd_simt_kernel<HG><<<dim3(nt, a.H / HG), kNT, sm, s>>>(a);
   return cudaGetLastError();
 }
 template <int HG>

@@ -27,6 +27,8 @@ struct FwdArgs {
   float* lse;               // [T, H]
   int T, H, topk;
   float scale;
+  // query rows [t0, t0 + nt) of this launch (nt < 0: all T rows)
+  int t0 = 0, nt = -1;
 };
 
 struct BwdArgs {

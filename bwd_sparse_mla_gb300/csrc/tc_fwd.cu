@@ -91,6 +91,7 @@ struct TcFwdParams {
   float* lse;
   uint32_t* status;
   int T, H, topk;                       // H <= 128 heads; rows H..127 of the tile are zero
+  int t0;                               // this launch handles query rows t0, t0 + 1, ...
   float c2;                             // scale * log2(e)
 };
 
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();          // 0 or 1
   const uint32_t peer = crank ^ 1u;
-  const int t = blockIdx.x >> 1;
+  const int t = p.t0 + (blockIdx.x >> 1);
   const int nch = 4 + (int)crank;                     // 64-dim key chunks of this CTA
   const int g0 = 4 * (int)crank;                      // first global chunk
   const int nblk = p.topk / kBK;           // blocks of the token's slot list
@@ -490,8 +491,10 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   float* xchg = tc_xchg_ptr();
   if (!xchg) return cudaErrorInvalidSymbol;
-  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.scale * kLog2e};
-  tc_fwd_h128_kernel<<<dim3(2 * a.T), dim3(kThreads), kSmemBytes, s>>>(p);
+  const int nt = a.nt < 0 ? a.T : a.nt;
+  if (nt == 0) return cudaSuccess;
+  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.t0, a.scale * kLog2e};
+  tc_fwd_h128_kernel<<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,20 @@ int sparse_mla_fwd(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* i
                    const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
                    smla_bf16_t* out, float* lse, void* stream);
 
+/*
+ * Forward over the query rows [t0, t0 + nt) only (an interface addition: the
+ * pages compute all rows in one call).  Same arguments and results as
+ * sparse_mla_fwd; q, indices, out and lse are still the full [T, ...]
+ * arrays, of which only rows t0 .. t0 + nt - 1 are read (q, indices) or
+ * written (out, lse); every kv row may be gathered.  A caller that streams
+ * q to the device in pieces computes each piece as soon as it has landed.
+ * The rows' results are bit-identical to those of sparse_mla_fwd.
+ * Needs 0 <= t0, 0 <= nt, t0 + nt <= T (else -EINVAL); nt = 0 launches nothing.
+ */
+int sparse_mla_fwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices,
+                        const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale, int t0, int nt,
+                        smla_bf16_t* out, float* lse, void* stream);
+
 /* Bytes of device workspace sparse_mla_bwd needs for these sizes (0 if the
  * sizes are invalid).  SMLA_DKV_ATOMIC: Delta = rowsum(dO * out), [T, H] fp32.
  * SMLA_DKV_DETERMINISTIC: Delta, the kv rows' sorted slot lists (about
@@ -124,6 +138,35 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
                    const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale,
                    int dkv_mode, smla_bf16_t* dq, float* dkv_f32, smla_bf16_t* dkv,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward contribution of the query rows [t0, t0 + nt) (an interface
+ * addition for callers that stream the step through the device in pieces),
+ * with dKV accumulated by fp32 atomic adds (SMLA_DKV_ATOMIC).
+ *   q, kv, out, dout, lse, indices, cu_seqlens, scale  as for sparse_mla_bwd
+ *            (full [T, ...] arrays; only rows t0 .. t0 + nt - 1 of q, out,
+ *            dout, lse and indices are read)
+ *   dq       rows t0 .. t0 + nt - 1 of [T, H, 576] bf16 are written, bit-
+ *            identical to those of sparse_mla_bwd
+ *   dkv_f32  [T, 1, 576] fp32: the rows' dKV contributions are ADDED; the
+ *            caller zeroes it once before the first range (e.g. with
+ *            cudaMemsetAsync) and may then cast it with sparse_mla_dkv_cast.
+ *            After all ranges of a step it equals sparse_mla_bwd's dkv_f32 up
+ *            to the order of the fp32 additions.
+ *   workspace, workspace_bytes  at least
+ *            sparse_mla_bwd_workspace_bytes(T, H, topk, SMLA_DKV_ATOMIC) bytes;
+ *            Delta of row t is kept at row t, so ranges that do not overlap
+ *            may share one workspace, on one stream or on several.
+ * Needs 0 <= t0, 0 <= nt, t0 + nt <= T (else -EINVAL); nt = 0 launches nothing.
+ */
+int sparse_mla_bwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_t* out,
+                        const smla_bf16_t* dout, const float* lse, const int32_t* indices,
+                        const int32_t* cu_seqlens, int T, int H, int topk, int B, float scale, int t0, int nt,
+                        smla_bf16_t* dq, float* dkv_f32, void* workspace, size_t workspace_bytes, void* stream);
+
+/* dkv [T, 1, 576] bf16 = round-to-nearest-even of dkv_f32 [T, 1, 576] fp32
+ * (the cast sparse_mla_bwd applies when its dkv is not NULL). */
+int sparse_mla_dkv_cast(const float* dkv_f32, smla_bf16_t* dkv, int T, void* stream);
 
 /*
  * Backward that allocates nothing (the pages have no counterpart: this is an

@@ -137,3 +137,43 @@ def test_topk_rejects_bad_arguments(lib):
     assert call(T=0) == 0
     assert lib.sparse_mla_topk(None, 64, 16, 64, FAKE, 1, 8, FAKE, None) == EINVAL
 
+
+
+def _fwd_rows(lib, T=16, t0=0, nt=16, q=FAKE, out=FAKE):
+    return lib.sparse_mla_fwd_rows(q, FAKE, FAKE, None, T, 8, 64, 1, 0.04, t0, nt, out, FAKE, None)
+
+
+def _bwd_rows(lib, T=16, t0=0, nt=16, ws_bytes=1 << 20, dkv=FAKE):
+    return lib.sparse_mla_bwd_rows(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, T, 8, 64, 1, 0.04, t0, nt, FAKE, dkv,
+                                   FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("call", [_fwd_rows, _bwd_rows])
+@pytest.mark.parametrize("t0,nt", [(-1, 4), (0, -1), (10, 7), (16, 1), (2**31 - 1, 2)])
+def test_row_ranges_outside_the_tokens_are_rejected(lib, call, t0, nt):
+    assert call(lib, t0=t0, nt=nt) == EINVAL
+    assert "t0" in capi.sparse_mla_last_error()
+
+
+@pytest.mark.parametrize("call", [_fwd_rows, _bwd_rows])
+def test_empty_row_range_is_a_noop(lib, call):
+    assert call(lib, t0=16, nt=0) == 0               # the range [T, T) is empty, and valid
+    assert call(lib, t0=3, nt=0) == 0
+    assert capi.sparse_mla_last_error() == ""
+
+
+def test_row_calls_check_pointers_and_workspace(lib):
+    assert _fwd_rows(lib, q=None) == EINVAL
+    assert "q must not be NULL" in capi.sparse_mla_last_error()
+    assert _fwd_rows(lib, out=MISALIGNED) == EINVAL
+    assert _bwd_rows(lib, dkv=None) == EINVAL
+    assert "dkv_f32 must not be NULL" in capi.sparse_mla_last_error()
+    assert _bwd_rows(lib, ws_bytes=16 * 8 * 4 - 1) == EINVAL     # Delta needs T * H fp32 values
+    assert "workspace too small" in capi.sparse_mla_last_error()
+
+
+def test_dkv_cast_checks(lib):
+    assert lib.sparse_mla_dkv_cast(FAKE, FAKE, -1, None) == EINVAL
+    assert lib.sparse_mla_dkv_cast(None, FAKE, 4, None) == EINVAL
+    assert lib.sparse_mla_dkv_cast(FAKE, MISALIGNED, 4, None) == EINVAL
+    assert lib.sparse_mla_dkv_cast(None, None, 0, None) == 0
