@@ -190,6 +190,25 @@ def run_reference(args):
 MODE_NAMES = {0: "atomic", 1: "deterministic (index-sorted segmented reduction)"}
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over the ranks of the default process
+    group (the values themselves without one): replicas report the slowest
+    rank's times."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_throughput(tokens_per_rank, world, ms):
+    """Whole-job tokens/s of `world` replicas that each processed
+    tokens_per_rank tokens, the slowest taking `ms` milliseconds."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -267,11 +286,8 @@ def run_ours(args):
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     ms = fwd_ms + bwd_ms
-    if world > 1:
-        t = torch.tensor([ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, fwd_ms, bwd_ms = [float(x) for x in t.tolist()]
-    value = world * T / (ms / 1e3)
+    ms, fwd_ms, bwd_ms = max_over_ranks([ms, fwd_ms, bwd_ms], dev)
+    value = replica_throughput(T, world, ms)
 
     # finite-output check of the last timed step (outside the timed region)
     finite = bool(torch.isfinite(lse).all()) and bool(torch.isfinite(dkv32).all())
@@ -332,10 +348,8 @@ def run_ours(args):
         e2e = run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu)
         e2e["matches_device_step"] = same_results(e2e.pop("_host"), (out, lse, dq, dkv), dev)
         if world > 1:
-            t = torch.tensor([e2e["ms_per_step"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = float(t.item())
-            e2e["value"] = world * T / (e2e["ms_per_step"] / 1e3)
+            e2e["ms_per_step"] = max_over_ranks([e2e["ms_per_step"]], dev)[0]
+            e2e["value"] = replica_throughput(T, world, e2e["ms_per_step"])
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
