@@ -531,6 +531,55 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
             "_host": (o_out, o_lse, o_dq, o_dkv)}
 
 
+def run_topk(args):
+    """Times the top-k index selection (sparse_mla_topk) alone on the workload's
+    sequence layout: seeded N(0,1) fp32 index scores [T, longest sequence],
+    each row reading its causal candidates; prints one JSON line (not the
+    step's line).  Its bound is HBM: every candidate score is read once."""
+    import torch
+    from bwd_sparse_mla_gb300 import capi
+    dev = torch.device("cuda", 0)
+    capi.load()
+    w = W.make_workload(args.config, values=False)
+    cu_np = np.asarray(w.cu_seqlens, dtype=np.int64)
+    if args.tokens:
+        T = min(args.tokens, w.T)
+        cu_np = np.minimum(cu_np, T)
+        cu_np = np.unique(cu_np)
+    else:
+        T = w.T
+    ncols = int(np.diff(cu_np).max())
+    cand = int(sum(min(p + 1, ncols) for s0, s1 in zip(cu_np[:-1], cu_np[1:]) for p in range(s1 - s0)))
+    cu = torch.from_numpy(cu_np.astype(np.int32)).to(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    scores = torch.randn(T, ncols, device=dev, generator=g)
+    idx = torch.empty((T, 1, w.topk), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        capi.sparse_mla_topk(scores, cu, w.topk, indices=idx)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        capi.sparse_mla_topk(scores, cu, w.topk, indices=idx)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.mean(times))
+    peaks, src = load_peaks()
+    gbs = cand * 4 / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "kernel": "sparse_mla_topk", "workload": w.name, "rows": T, "ncols": ncols, "topk": w.topk,
+        "candidates": cand, "ms": ms, "steps": args.steps, "warmup": args.warmup,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "peak_source": src,
+                     "algorithmic_bytes": cand * 4},
+        "l2": "flushed before every timed call (256 MiB write)"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -547,10 +596,14 @@ def main():
                     help="dKV accumulation of the timed backward: 0 = fp32 atomics, 1 = sorted segmented reduction")
     ap.add_argument("--other-mode-steps", type=int, default=2,
                     help="after the timed region, time the backward in the other dKV mode for this many steps")
+    ap.add_argument("--topk-only", action="store_true",
+                    help="time only the top-k index selection on the workload's sequence layout")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.topk_only:
+        run_topk(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
