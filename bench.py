@@ -265,8 +265,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    log_dir = os.path.join(ROOT, "gpurun_out")
-    sampler = ClockSampler(bus_id_of(dev), os.path.join(log_dir, "clocks.csv") if os.path.isdir(log_dir) else None)
+    sampler = ClockSampler(bus_id_of(dev), args.clocks_csv)
     launches0 = capi.sparse_mla_launch_count()
     wall0 = time.perf_counter()
     for k in range(args.steps):
@@ -596,6 +595,8 @@ def main():
                     help="dKV accumulation of the timed backward: 0 = fp32 atomics, 1 = sorted segmented reduction")
     ap.add_argument("--other-mode-steps", type=int, default=2,
                     help="after the timed region, time the backward in the other dKV mode for this many steps")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--topk-only", action="store_true",
                     help="time only the top-k index selection on the workload's sequence layout")
     args = ap.parse_args()
