@@ -462,12 +462,15 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk), 256), dtype=torch.uint8, device=dev)
     cs = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # ranges alternate between two compute streams: they are independent (their dKV
+    # contributions add commutatively), so one range's tail overlaps the next one's work
+    comp = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
     bounds = [round(i * T / E2E_CHUNKS) for i in range(E2E_CHUNKS + 1)]
     ranges = [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(E2E_CHUNKS) if bounds[i + 1] > bounds[i]]
 
     def one(start):
         ev = lambda: torch.cuda.Event()  # noqa: E731
-        ev_meta, ev_cast, ev_done = ev(), ev(), ev()
+        ev_meta, ev_zero, ev_cast, ev_done = ev(), ev(), ev(), ev()
         ev_q, ev_do, ev_f, ev_b = ([ev() for _ in ranges] for _ in range(4))
         s_in.wait_event(start)
         with torch.cuda.stream(s_in):
@@ -481,16 +484,24 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
             for c, (t0, nt) in enumerate(ranges):       # overlaps the forward
                 d_do[t0:t0 + nt].copy_(hdo[t0:t0 + nt], non_blocking=True)
                 ev_do[c].record(s_in)
-        cs.wait_event(ev_meta)
+        cs.wait_event(start)
         d_dkv32.zero_()                                # the row-range backward adds into it
+        ev_zero.record(cs)
         for c, (t0, nt) in enumerate(ranges):
-            cs.wait_event(ev_q[c])
-            capi.sparse_mla_fwd_rows(d_q, d_kv, d_idx, d_cu, w.scale, t0, nt, d_out, d_lse)
-            ev_f[c].record(cs)
+            st = comp[c % 2]
+            st.wait_event(ev_meta)
+            st.wait_event(ev_q[c])
+            capi.sparse_mla_fwd_rows(d_q, d_kv, d_idx, d_cu, w.scale, t0, nt, d_out, d_lse, stream=st)
+            ev_f[c].record(st)
         for c, (t0, nt) in enumerate(ranges):
-            cs.wait_event(ev_do[c])
-            capi.sparse_mla_bwd_rows(d_q, d_kv, d_out, d_do, d_lse, d_idx, d_cu, w.scale, t0, nt, d_dq, d_dkv32, ws)
-            ev_b[c].record(cs)
+            st = comp[c % 2]
+            st.wait_event(ev_do[c])
+            st.wait_event(ev_zero)
+            capi.sparse_mla_bwd_rows(d_q, d_kv, d_out, d_do, d_lse, d_idx, d_cu, w.scale, t0, nt, d_dq, d_dkv32, ws,
+                                     stream=st)
+            ev_b[c].record(st)
+        for c in range(len(ranges)):
+            cs.wait_event(ev_b[c])
         capi.sparse_mla_dkv_cast(d_dkv32, d_dkv)
         ev_cast.record(cs)
         with torch.cuda.stream(s_out):
@@ -524,9 +535,9 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     # for bit, dkv (bf16 of an fp32 sum in another order) within one bf16 step
     return {"value": T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps, "chunks": len(ranges), "dkv_mode": "atomic",
-            "overlap": f"streamed in {len(ranges)} ranges of query rows: q / indices upload overlaps the forward "
-                       "of earlier ranges, dO upload the forward, out / lse and dq download later ranges' work "
-                       "(separate copy streams)",
+            "overlap": f"streamed in {len(ranges)} ranges of query rows on two alternating compute streams: q / "
+                       "indices upload overlaps the forward of earlier ranges, dO upload the forward, out / lse and "
+                       "dq download later ranges' work (separate copy streams)",
             "_host": (o_out, o_lse, o_dq, o_dkv)}
 
 
