@@ -150,6 +150,8 @@ __device__ __forceinline__ bool drain_any(uint32_t sb, uint32_t tl, uint32_t tm_
 // the softmax warps (the rest): the exchange warps' other work per block is lighter
 constexpr int kXchgCols = 20;
 
+// kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
+template <bool kAllHeads>
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_bwd_h128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        TcBwdParams p) {
@@ -399,12 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       // add the peer's partial rows (published by its exchange warps)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + xb), (i >> 1) & 1, abort_flag, p.status))))
         break;
+      // heads past H (zero q and dO rows: exactly 0 partials) are not exchanged
       const float4* rd = xpeer + xb * (kXchgBufFloats / 4);
+      if (kAllHeads || real) {
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
-        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
-        dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
+        for (int v = 0; v < 8; ++v) {
+          const float4 a = ld_cg_v4(rd + v * 128), c = ld_cg_v4(rd + (8 + v) * 128);
+          s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+          dp[4 * v] += c.x; dp[4 * v + 1] += c.y; dp[4 * v + 2] += c.z; dp[4 * v + 3] += c.w;
+        }
       }
       mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
@@ -500,10 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
                                                                    abort_flag, p.status))))
         break;
       float4* wr = xmine + xb * (kXchgBufFloats / 4);
+      if (kAllHeads || L < p.H) {       // heads past H have exactly 0 partials and are not exchanged
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-        wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
+        for (int v = 0; v < 8; ++v) {
+          wr[v * 128] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+          wr[(8 + v) * 128] = make_float4(dp[4 * v], dp[4 * v + 1], dp[4 * v + 2], dp[4 * v + 3]);
+        }
       }
       mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
       // row list of block i (the softmax warps read it too), then the exchange
@@ -574,13 +581,18 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
   uint32_t* status = tc_status_ptr();
   float* xchg = tc_xchg_ptr();
   if (!status || !xchg) return cudaErrorInvalidSymbol;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool all = a.H == 128;
+  cudaError_t e = cudaFuncSetAttribute(all ? tc_bwd_h128_kernel<true> : tc_bwd_h128_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nt = a.nt < 0 ? a.T : a.nt;
   if (nt == 0) return cudaSuccess;
   TcBwdParams p{a.kv,   xchg,   a.indices, a.lse, a.delta, a.dq,    a.dkv32,
                 a.gbuf, status, a.T,       a.H,   a.topk,  a.t0,    a.scale, a.scale * kLog2e};
-  tc_bwd_h128_kernel<<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
+  if (all)
+    tc_bwd_h128_kernel<true><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
+  else
+    tc_bwd_h128_kernel<false><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,8 @@ struct TcFwdParams {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
+// kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
+template <bool kAllHeads>
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_fwd_h128_kernel(TcFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -317,17 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       if (k2 >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + b), (k2 - 1) & 1, abort_flag,
                                                                    p.status))))
         break;
+      // rows past H (zero q rows: their partial scores are exactly 0 on both
+      // CTAs) skip the exchange; every thread still arrives
+      const bool xreal = kAllHeads || h < p.H;
       float4* wr = xmine + b * (kXchgBufFloats / 4);
+      if (xreal) {
 #pragma unroll
-      for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(s[4 * v4], s[4 * v4 + 1], s[4 * v4 + 2], s[4 * v4 + 3]);
+        for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(s[4 * v4], s[4 * v4 + 1], s[4 * v4 + 2], s[4 * v4 + 3]);
+      }
       mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), k2 & 1, abort_flag, p.status))))
         break;
       const float4* rd = xpeer + b * (kXchgBufFloats / 4);
+      if (xreal) {
 #pragma unroll
-      for (int v4 = 0; v4 < 16; ++v4) {
-        const float4 o = ld_cg_v4(rd + v4 * 128);
-        s[4 * v4] += o.x; s[4 * v4 + 1] += o.y; s[4 * v4 + 2] += o.z; s[4 * v4 + 3] += o.w;
+        for (int v4 = 0; v4 < 16; ++v4) {
+          const float4 o = ld_cg_v4(rd + v4 * 128);
+          s[4 * v4] += o.x; s[4 * v4 + 1] += o.y; s[4 * v4 + 2] += o.z; s[4 * v4 + 3] += o.w;
+        }
       }
       mbar_arrive_remote(xempty_peer + 8 * b);    // the peer may reuse that buffer
       // slot validity of this block (written by the producer before it armed KV_FULL)
@@ -487,14 +496,19 @@ cudaError_t launch_wait_selftest(cudaStream_t s) {
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   uint32_t* status = tc_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_h128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool all = a.H == 128;
+  cudaError_t e = cudaFuncSetAttribute(all ? tc_fwd_h128_kernel<true> : tc_fwd_h128_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   float* xchg = tc_xchg_ptr();
   if (!xchg) return cudaErrorInvalidSymbol;
   const int nt = a.nt < 0 ? a.T : a.nt;
   if (nt == 0) return cudaSuccess;
   TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.t0, a.scale * kLog2e};
-  tc_fwd_h128_kernel<<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
+  if (all)
+    tc_fwd_h128_kernel<true><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
+  else
+    tc_fwd_h128_kernel<false><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
