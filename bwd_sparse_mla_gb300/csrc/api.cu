@@ -363,31 +363,23 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
 // array instead, so the caller passes only inputs and outputs.
 namespace {
 
+// counter of sparse_mla_check_indices (one word per device) and the host lock
+// that serialises its users
+__device__ unsigned long long g_check_counter;
+std::mutex g_check_mu;
+
 constexpr size_t kNoAllocMaxRows = size_t(1) << 23;   // T * H <= 8,388,608 values (32 MiB of fp32)
 __device__ __align__(256) float g_noalloc_delta[kNoAllocMaxRows];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
 // In host code g_noalloc_delta names a host-side stand-in, not the device
-// array, so its device address is looked up once per device (with that device
-// current) and cached.  This is the only set-up step.
+// array, so its device address is looked up with the caller's device current.
+// The lookup is made on every call (it is a cheap runtime query), so the
+// address is always the one of the current device and context.
 int noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kNoAllocMaxDevices)
-    return fail(-ENOTSUP, "device %d is beyond the %d devices the no-allocation path tracks", dev,
-                kNoAllocMaxDevices);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_delta);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_delta);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+  *out = static_cast<float*>(p);
   return 0;
 }
 
@@ -451,9 +443,14 @@ int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int3
   if (cu_seqlens == nullptr) return fail(-EINVAL, "cu_seqlens must not be NULL");
   if (int r = check_device()) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned long long* counter = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&counter), sizeof(*counter), s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+  // the count goes to a counter word inside the library (one per device); the
+  // call holds a host lock from zeroing it to reading it back, so concurrent
+  // calls from other host threads wait instead of sharing it
+  std::lock_guard<std::mutex> lock(g_check_mu);
+  void* cp = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&cp, g_check_counter);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(index-check counter)");
+  unsigned long long* counter = static_cast<unsigned long long*>(cp);
   unsigned long long host = 0;
   e = cudaMemsetAsync(counter, 0, sizeof(*counter), s);
   if (e == cudaSuccess) {
@@ -461,8 +458,6 @@ int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int3
     if (e == cudaSuccess) count_launches(1);
   }
   if (e == cudaSuccess) e = cudaMemcpyAsync(&host, counter, sizeof(host), cudaMemcpyDeviceToHost, s);
-  cudaError_t e2 = cudaFreeAsync(counter, s);
-  if (e == cudaSuccess) e = e2;
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_check_indices");
   *n_bad = (int64_t)host;

@@ -180,10 +180,11 @@ int sparse_mla_dkv_cast(const float* dkv_f32, smla_bf16_t* dkv, int T, void* str
  * every GPU that loads the library holds until the process exits.
  *   - T * H must be <= 8,388,608 (e.g. T = 65536 at H = 128); larger sizes
  *     return -EINVAL with a message and launch nothing.
- *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
- *     call on each device (with that device current) looks up the device
- *     address of the array once; make that first call before any stream
- *     capture.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  Every call
+ *     looks up the device address of the array for the current device (a
+ *     runtime query that allocates nothing); the first call on a device may
+ *     also load the library's kernels there, so make that first call before
+ *     any stream capture.
  *   - All calls share the one array and it keeps the last call's contents
  *     (each call rewrites the part it uses before reading it).  Calls that
  *     overlap on the GPU -- on different streams, or from different host
@@ -199,8 +200,10 @@ int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const sm
  * -1).  Counts the entries of indices [T, 1, topk] that are neither -1 nor a
  * row of their own query's sequence [cu_seqlens[b], cu_seqlens[b+1]).
  * cu_seqlens [B+1] int32 (device) must start at 0, be non-decreasing and end
- * at T.  Writes the count to *n_bad (HOST pointer).  This call allocates a
- * small device counter on `stream` and synchronizes that stream.
+ * at T.  Writes the count to *n_bad (HOST pointer).  The count is taken in a
+ * counter word inside the library (one per device, nothing is allocated);
+ * the call synchronizes `stream` before it returns and holds a host lock
+ * meanwhile, so calls from several host threads run one after another.
  */
 int sparse_mla_check_indices(const int32_t* indices, int T, int topk, const int32_t* cu_seqlens,
                              int B, int64_t* n_bad, void* stream);

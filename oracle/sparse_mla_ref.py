@@ -21,7 +21,7 @@ Sources (web pages; cited by title and section):
   [PR17]   Megatron-Bridge PR #17, "GLM-5 DSA option: tilelang (2/2)" --
            "Bug fixes" (top-k padded to the fixed width with -1; thd layout).
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
   * valid slot = index in [0, T); -1 and every other out-of-range value are
     padding and contribute nothing (the pages mask `index != -1` and clamp).
   * duplicate indices in one row count once per slot (a multiset).

@@ -9,7 +9,7 @@ can see in its own sequence (`_original_topk`), and the index list is padded
 to the fixed width `topk` with -1 (the padding the sparse-MLA kernels then
 mask, miles PR #2079 item 2).
 
-Readings of points the page leaves open (each also listed in the design doc):
+Readings of points the page leaves open:
   * candidates of query t (position p = t - s0 in its sequence starting at
     packed row s0) are the causal keys s0 .. t, with scores
     scores[t, 0 .. p]; the indices written are packed kv rows s0 + c.

@@ -34,6 +34,7 @@ def check(path, rows: int = 256, full: bool = False, seed: int = 0, device="cuda
     report = dict(counts)
     report["dq_rows_checked"] = int(sample.size)
     report["dq_max_abs_diff_finite"] = float(np.abs(dq_g - dq_ref)[fin].max()) if fin.any() else 0.0
+    report["dq_max_abs_ref"] = float(np.abs(dq_ref).max()) if dq_ref.size else 0.0
     if sample.size == T:       # every row's contribution is in the oracle's dkv
         dkv_g = dkv32.cpu().numpy().astype(np.float64).reshape(T, -1)
         fin = np.isfinite(dkv_g)

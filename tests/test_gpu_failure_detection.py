@@ -38,5 +38,5 @@ def test_bounded_wait_times_out_and_context_survives(cuda_device):
     assert capi.sparse_mla_device_status() == 0
     rows = list(range(0, w.T, 7))
     o_ref, lse_ref = ref.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, rows=rows)
-    assert_close("out", to_f64(out)[rows], o_ref)
+    assert_close("out", to_f64(out)[rows], o_ref, kind="bf16")
     assert_close("lse", to_f64(lse)[rows], lse_ref)

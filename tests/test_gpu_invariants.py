@@ -99,7 +99,7 @@ def test_permuting_a_row_keeps_out_and_lse(case):
     idx = torch.from_numpy(np.ascontiguousarray(idx_np.reshape(w.T, 1, -1))).to(d["q"].device)
     out2, lse2, *_ = _run(d, w.scale, indices=idx)
     out_ref, lse_ref = orc.sparse_mla_fwd(w.q, w.kv, idx_np, w.scale)
-    assert_close("out(perm)", to_f64(out2), out_ref)
+    assert_close("out(perm)", to_f64(out2), out_ref, kind="bf16")
     assert_close("lse(perm)", to_f64(lse2), lse_ref)
 
 

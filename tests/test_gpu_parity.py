@@ -12,7 +12,7 @@ import torch
 import oracle.sparse_mla_ref as orc
 from bwd_sparse_mla_gb300 import capi
 from bwd_sparse_mla_gb300 import workloads as W
-from tests.gpu_helpers import (LSE_EMPTY_F32, MAX_ABS, assert_close, device_inputs, empty_rows,
+from tests.gpu_helpers import (LSE_EMPTY_F32, assert_close, device_inputs, empty_rows,
                                f64_to_bf16_dev, oracle_inputs, to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -63,7 +63,7 @@ def test_fwd_small(small):
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
     out_g, lse_g = to_f64(out), to_f64(lse)
-    assert_close("out", out_g, out_ref)
+    assert_close("out", out_g, out_ref, kind="bf16")
     assert_close("lse", lse_g, lse_ref)
     er = empty_rows(w)
     assert er.size > 0
@@ -80,7 +80,7 @@ def test_bwd_small(small):
                                            d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
     dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, to_f64(out_in), dout, to_f64(lse_in), w.indices, w.scale)
-    assert_close("dq", to_f64(dq), dq_ref)
+    assert_close("dq", to_f64(dq), dq_ref, kind="bf16")
     assert_close("dkv", to_f64(dkv32).reshape(w.T, -1), dkv_ref)
     # the bf16 copy is the round-to-nearest-even cast of the fp32 accumulator
     assert torch.equal(dkv16, dkv32.to(torch.bfloat16))
@@ -93,31 +93,21 @@ def test_bwd_small(small):
 
 
 def test_fwd_bwd_chain_small(small):
-    """GPU forward feeding GPU backward vs the oracle chain.  The backward's
-    `out` argument is bf16 in this interface, so the oracle chain hands its
-    backward the oracle output rounded to bf16 as well: with a near one-hot
-    softmax, dS = P (dP - Delta) cancels and Delta inherits the bf16 rounding
-    of `out`, which no kernel can undo."""
+    """GPU forward feeding GPU backward, at every head count and logit scale.
+
+    The forward's out / lse are compared with the oracle forward.  The backward
+    takes out and lse as given inputs (the kernel call in slime issue #2201,
+    "Strongest repro evidence", passes tl_out and tl_lse), so its results are
+    compared with the oracle backward given the same bf16 out and fp32 lse."""
     w, d, (q, kv, dout), (out_ref, lse_ref) = small
-    if w.q_std != 1.0:
-        pytest.skip("q ~ N(0, 8^2): the near one-hot softmax makes dS = P (dP - Delta) cancel, so the "
-                    "chained dq inherits the forward's bf16 output rounding; the backward alone is "
-                    "checked on identical inputs in test_bwd_small")
-    out_bf16 = torch.tensor(out_ref, dtype=torch.float64).to(torch.bfloat16).double().numpy()
-    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, out_bf16, dout, lse_ref, w.indices, w.scale)
-    # how far the bf16 rounding of `out` alone moves the oracle's own gradients: where kv rows
-    # are named by hundreds of queries this exceeds the bound, and no comparison through the
-    # bf16 `out` of the interface can then be held to it
-    dq_x, dkv_x = orc.sparse_mla_bwd(q, kv, out_ref, dout, lse_ref, w.indices, w.scale)
-    own = max(float((np.abs(a - b) / np.maximum(1.0, np.abs(b))).max()) for a, b in ((dq_x, dq_ref), (dkv_x, dkv_ref)))
-    if own > MAX_ABS:
-        pytest.skip(f"rounding `out` to bf16 moves the oracle's own dq/dkv by {own:.2e} (relative to max(1, |ref|)), "
-                    f"more than the {MAX_ABS} bound; the backward alone is checked in test_bwd_small")
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
     dq, dkv32, _ = capi.sparse_mla_bwd(d["q"], d["kv"], out, d["dout"], lse, d["indices"],
                                        d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
-    assert_close("dq(chain)", to_f64(dq), dq_ref)
+    assert_close("out(chain)", to_f64(out), out_ref, kind="bf16")
+    assert_close("lse(chain)", to_f64(lse), lse_ref)
+    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, to_f64(out), dout, to_f64(lse), w.indices, w.scale)
+    assert_close("dq(chain)", to_f64(dq), dq_ref, kind="bf16")
     assert_close("dkv(chain)", to_f64(dkv32).reshape(w.T, -1), dkv_ref)
 
 
@@ -135,7 +125,7 @@ def test_full_size_sampled(cfg, dkv_mode, cuda_device):
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     out_ref, lse_ref = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, rows=rows)
     rt = torch.from_numpy(rows).to(cuda_device)
-    assert_close("out", to_f64(out[rt]), out_ref)
+    assert_close("out", to_f64(out[rt]), out_ref, kind="bf16")
     assert_close("lse", to_f64(lse[rt]), lse_ref)
     er = empty_rows(w)
     assert np.all(to_f64(out[torch.from_numpy(er).to(cuda_device)]) == 0.0)
@@ -154,7 +144,7 @@ def test_full_size_sampled(cfg, dkv_mode, cuda_device):
     torch.cuda.synchronize()
     dq_ref, dkv_ref = orc.sparse_mla_bwd(w.q, w.kv, to_f64(out_in[rt]), w.dout, to_f64(lse_in[rt]),
                                          w.indices, w.scale, rows=rows)
-    assert_close("dq", to_f64(dq[rt]), dq_ref)
+    assert_close("dq", to_f64(dq[rt]), dq_ref, kind="bf16")
     # rows outside the sample have dO = 0, hence dS = 0 and dq exactly 0
     nz = torch.cat([torch.count_nonzero(dq[i:i + 4096], dim=(1, 2)) for i in range(0, w.T, 4096)])
     nz[rt] = 0

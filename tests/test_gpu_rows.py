@@ -88,6 +88,6 @@ def test_bwd_rows_match_the_whole_call_and_the_oracle(case):
     assert torch.equal(_bits(dkv16_full_cast), _bits(dkv16))       # the cast the whole call applies
     assert torch.equal(dkv16_r, dkv32_r.to(torch.bfloat16))
     dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, to_f64(out_in), dout, to_f64(lse_in), w.indices, w.scale)
-    assert_close("dq", to_f64(dq_r), dq_ref)
+    assert_close("dq", to_f64(dq_r), dq_ref, kind="bf16")
     assert_close("dkv", to_f64(dkv32_r).reshape(w.T, -1), dkv_ref)
     assert np.isfinite(to_f64(dkv16_r)).all()

@@ -57,6 +57,6 @@ def test_topk_indices_feed_sparse_mla(cuda_device):
     out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], idx, d["cu_seqlens"], w.scale)
     torch.cuda.synchronize()
     out_ref, lse_ref = orc.sparse_mla_fwd(w.q, w.kv, idx_ref, w.scale)
-    assert_close("out", to_f64(out), out_ref)
+    assert_close("out", to_f64(out), out_ref, kind="bf16")
     assert_close("lse", to_f64(lse), lse_ref)
     assert capi.sparse_mla_check_indices(idx, d["cu_seqlens"]) == 0     # every index in its own sequence

@@ -9,7 +9,7 @@ import torch
 
 import oracle.sparse_mla_ref as orc
 from bwd_sparse_mla_gb300 import workloads as W
-from tests.gpu_helpers import device_inputs, f64_to_bf16_dev, oracle_inputs
+from tests.gpu_helpers import MAX_ABS, device_inputs, f64_to_bf16_dev, oracle_inputs
 
 
 def _bf16(bits):
@@ -63,4 +63,7 @@ def test_replay_matches_direct_call_and_oracle(H, tmp_path, cuda_device):
     rep = replay_check.check(path, rows=w.T)
     assert rep["dq_nonfinite"] == 0 and rep["dkv_nonfinite"] == 0
     assert rep["dq_rows_checked"] == w.T
-    assert rep["dq_max_abs_diff_finite"] < 2e-2 and rep["dkv_max_abs_diff_finite"] < 2e-2 * max(1.0, float(dkv32.abs().max()))
+    # the oracle comparison on the finite overlap, with the stated bounds: dq is a bf16
+    # output (its values here stay below magnitude 8, so the bound is 2e-2), dkv fp32
+    assert rep["dq_max_abs_ref"] < 8.0
+    assert rep["dq_max_abs_diff_finite"] <= MAX_ABS and rep["dkv_max_abs_diff_finite"] <= MAX_ABS

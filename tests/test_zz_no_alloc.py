@@ -30,10 +30,12 @@ def test_noalloc_matches_workspace_backward_twice(H, cuda_device):
     torch.cuda.synchronize()
     lib = capi.load()
     P = ctypes.c_void_p
-    for _ in range(2):   # two calls in a row share the scratch array
+    for call in range(2):   # two calls in a row share the scratch array
         dq = torch.full_like(dq_ref, float("nan"))
         dkv32 = torch.full_like(dkv_ref, float("nan"))
         dkv16 = torch.full_like(dkv16_ref, float("nan"))
+        torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
         rc = lib.sparse_mla_bwd_noalloc(
             P(d["q"].data_ptr()), P(d["kv"].data_ptr()), P(out.data_ptr()), P(d["dout"].data_ptr()),
             P(lse.data_ptr()), P(d["indices"].data_ptr()), P(d["cu_seqlens"].data_ptr()), w.T, w.H, w.topk,
@@ -41,6 +43,10 @@ def test_noalloc_matches_workspace_backward_twice(H, cuda_device):
             P(torch.cuda.current_stream().cuda_stream))
         assert rc == 0, capi.sparse_mla_last_error()
         torch.cuda.synchronize()
+        after = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
+        if call == 1:   # the first call on a device may load the library's kernels there
+            # nothing was allocated: torch's allocator and the device's free memory are unchanged
+            assert after == before, f"device memory changed across the call: {before} -> {after}"
         # dq is written by the same kernel with the same inputs: identical
         assert torch.equal(dq, dq_ref)
         # dkv is an fp32 atomic accumulation: equal up to summation order
