@@ -1,39 +1,36 @@
 // Tensor-core (tcgen05) forward for up to 128 heads (fewer heads run as a
 // 128-row tile whose rows past H are zero).
 //
-// Work split: a cluster of two CTAs handles one query token.  The 576-wide
-// key dimension is split between them (CTA 0: dims [0,256), CTA 1: dims
-// [256,576)), and so is the 512-wide value/output dimension (CTA 0: [0,256),
-// CTA 1: [256,512)).  Each CTA gathers only its own columns of the named KV
-// rows, so the pair reads every gathered byte exactly once, and each CTA
-// holds an O accumulator of 128 heads x 256 dims (256 TMEM columns).  The
-// partial scores of the two halves are exchanged through an L2 scratch and
-// summed in both CTAs (a + b == b + a, so both see bit-identical scores and
-// take identical softmax decisions).
+// Work split: a cluster of two CTAs works through a strided list of query
+// tokens (a persistent kernel: one cluster per pair of SMs), with different
+// roles, so that no fp32 partial result ever crosses between the CTAs.
 //
-// Per block of 64 top-k slots:
-//   producer warps: read the 64 indices (one block ahead), mask them (valid
-//                   iff 0 <= idx < T) and gather this CTA's columns of the
-//                   named rows with 16-byte cp.async into 128B-swizzled shared
-//                   memory; a padding slot copies zero bytes and gets an
-//                   exact-zero K/V row (the clamp + mask of the miles PR #2079
-//                   fix, implementation breakdown item 2);
-//   MMA thread    : S_half = Q_half K_half^T  (M=128 heads, N=64, K=256|320)
-//                   into one of two TMEM score buffers, and O += P V_half
-//                   (M=128, N=256, K=64), each issued as soon as its inputs
-//                   are ready;
-//   two groups of four warps, one thread per head, take alternate blocks:
-//                   load the 64 partial scores, write them to this SM's slot
-//                   of the L2 exchange scratch, signal the peer CTA through
-//                   its mbarrier, add the peer's partials, mask padding to
-//                   -inf and run the online softmax in the exp2 domain with a
-//                   lazily updated running max (handed from group to group
-//                   through shared memory), rescale O in TMEM when the max
-//                   moves, and write P (bf16) for the PV MMA.  One group's
-//                   exchange overlaps the other's softmax.  At the end the sum
-//                   of exponentials is floored at 1e-30 (PR #2079 forward
-//                   fragment), so a row with no valid slot gets out = 0 and
-//                   LSE = ln(1e-30).
+//   score CTA (cluster rank 0) holds the current token's q (128 heads x 576
+//     dims, bf16) in TMEM as the A operand and gathers the full 576-wide KV
+//     rows named by each block of 64 top-k slots.  Per block it computes the
+//     complete scores S = q K^T (M = 128 heads, N = 64 slots, K = 576).  Two
+//     softmax groups (one thread per head each) take alternate blocks: padding
+//     slots are masked to -inf, the running max moves lazily (only when a
+//     block max exceeds it by more than 8 in the log2 domain) and passes from
+//     group to group in block order, P = exp2(S*scale*log2e - m) is rounded to
+//     bf16.  P and the block's per-head rescale factors are copied into the
+//     output CTA's shared memory with one distributed-shared-memory bulk copy
+//     per block.  At the end of a token the sum of exponentials is floored at
+//     1e-30 (miles PR #2079 summary, forward fragment), so a row with no valid
+//     slot gets LSE = ln(1e-30).
+//
+//   output CTA (cluster rank 1) holds O (128 heads x 512 dims, fp32) in all of
+//     its TMEM.  It gathers the 512-wide value part of the same rows, rescales
+//     the O rows whose running max moved, and issues O += P V (M = 128,
+//     N = 256, K = 64, twice).  At the end of a token O is divided by the sum
+//     of the bf16-rounded weights (so the rounding of P cancels in `out`) and
+//     written as bf16; a row with no valid slot is written as exact zeros.
+//
+// Both CTAs gather with 16-byte cp.async into rings of 128B-swizzled units
+// that flow from one token into the next; a padding slot copies zero bytes
+// and gets an exact-zero K/V row (the clamp + mask of the miles PR #2079 fix,
+// implementation breakdown item 2).  Blocks whose 64 slots are all padding
+// contribute nothing and are skipped by both CTAs.
 #include <cuda.h>
 
 #include "smla_common.cuh"
@@ -45,59 +42,265 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
-constexpr int kProducers = 64;          // warps 0..1 gather, warp 2 MMA, warps 3..10 two exchange + softmax groups
-constexpr int kMmaWarp = 2;
-constexpr int kGroup0 = 3;
-constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 8 rows, one 16-byte piece of each chunk
-constexpr int kThreads = kProducers + 32 + 128 + 128;
-constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of a KV block
-constexpr int kStageBytes = 5 * kChunkKV;
+constexpr int kProducers = 128;         // warps 0..3 gather
+constexpr int kMmaWarp = 4;             // warp 4: lane 0 issues the MMAs (and the warp owns TMEM), lane 1 moves P
+constexpr int kRowWarp0 = 5;            // warps 5..8 (and 9..12 in the score CTA): one thread per head
+constexpr int kThreads = 416;
+constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4 rows, one 16-byte piece of each chunk
+constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of the 64 rows of a block (8 KiB)
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
 constexpr int kMaxBlocks = kTcMaxTopk / kBK;
+constexpr int kNS = 3;                  // score CTA: P staging buffers
+constexpr int kNP = 3;                  // output CTA: P buffers
+constexpr int kMaskRing = 4;            // score CTA: slot-validity masks of the blocks in flight
+constexpr int kProdBar = 1;             // named barrier of the producer warps
 
-// shared memory map (offsets from a 1024-aligned base); Q lives in TMEM
-constexpr int kStages = 5;
-constexpr int SM_KV = 0;                           // kStages stages
-constexpr int SM_P = SM_KV + kStages * kStageBytes;
-constexpr int SM_MASK = SM_P + 128 * 128;          // kStages x u64
-constexpr int SM_STATE = SM_MASK + 8 * kStages;    // running max and sums, 128 heads x float4
-constexpr int SM_BFLAG = SM_STATE + 128 * 16;      // per block: holds a valid slot (u8)
-constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;     // blocks with a valid slot, in order (u16)
-constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;    // their number
-constexpr int SM_BAR = SM_NB + 8;
-// S_FULL, X_FULL, X_EMPTY, ST_FULL and O_DONE come in pairs indexed by block parity:
-// each is then waited on only by one group, one phase at a time
-enum Bar { KV_FULL = 0, KV_EMPTY = kStages, Q_FULL = 2 * kStages, S_FULL, S_FREE = S_FULL + 2, X_FULL,
-           X_EMPTY = X_FULL + 2, ST_FULL = X_EMPTY + 2, P_FULL = ST_FULL + 2, O_DONE, NBAR = O_DONE + 2 };
-constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
+// KV rows are gathered into rings of units: a unit is kUnitCh 64-dim chunks of
+// the 64 rows of a block (128B-swizzled, 8 KiB per chunk, chunks contiguous).
+// A unit is refilled as soon as the MMAs that read it complete, so the gathers
+// stay in flight continuously, across token boundaries.
+//   score CTA:  units of 3 chunks (24 KiB), 3 per block (the 576-wide K rows)
+//   output CTA: units of 4 chunks (32 KiB), 2 per block (the 512-wide V rows;
+//               one unit is the B operand of one N = 256 PV MMA)
+constexpr int kSUnitCh = 3, kSUnits = 3, kSRing = 7;
+constexpr int kOUnitCh = 4, kOUnits = 2, kORing = 5;
+
+// one P buffer: 128 heads x 64 slots bf16 (128B swizzle, the PV MMA's A
+// operand), then the 128 rescale factors of the block
+constexpr int kPBytes = 128 * 128;
+constexpr int kPXBytes = kPBytes + 128 * 4;              // what one block hands over (16896 B)
+constexpr int kPBufStride = 17 * 1024;                   // 1024-aligned buffer stride
+// score CTA: K ring, P staging, the running state, the mask ring
+constexpr int SM_K = 0;
+constexpr int SM_STG = SM_K + kSRing * kSUnitCh * kChunkKV;
+constexpr int SM_STATE = SM_STG + kNS * kPBufStride;     // 128 heads x float4 (m, l, l_bf)
+constexpr int SM_MASK = SM_STATE + 128 * 16;             // kMaskRing x u64
+constexpr int kScoreEnd = SM_MASK + 8 * kMaskRing;
+// output CTA: V ring, P buffers, the final sums of two tokens
+constexpr int SM_V = 0;
+constexpr int SM_P = SM_V + kORing * kOUnitCh * kChunkKV;
+constexpr int SM_LBF = SM_P + kNP * kPBufStride;         // 2 x 128 floats from the score CTA
+constexpr int kOutEnd = SM_LBF + 2 * 512;
+// common to both roles: the token ring (block count of the two newest tokens),
+// the producers' per-token block flags and list
+constexpr int SM_TOK = kScoreEnd > kOutEnd ? kScoreEnd : kOutEnd;   // 2 x int
+constexpr int SM_BFLAG = SM_TOK + 16;                    // per block: holds a valid slot (u8)
+constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;          // blocks with a valid slot, in order (u16)
+constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;
+constexpr int SM_BAR = (SM_NB + 8 + 7) & ~7;
+// barriers: the same slots carry role-specific meanings
+enum ScoreBar { KV_FULL = 0, KV_EMPTY = kSRing, M_FULL = 2 * kSRing, M_EMPTY = M_FULL + kMaskRing,
+                Q_FULL = M_EMPTY + kMaskRing, Q_EMPTY, S_FULL, S_FREE = S_FULL + 2, ST_FULL = S_FREE + 2,
+                STG_FULL = ST_FULL + 2, STG_FREE = STG_FULL + kNS, P_FREE = STG_FREE + kNS, L_EMPTY = P_FREE + kNP,
+                TOK_FULL_S = L_EMPTY + 2, TOK_EMPTY_S = TOK_FULL_S + 2, NBAR_S = TOK_EMPTY_S + 2 };
+enum OutBar { V_FULL = 0, V_EMPTY = kORing, P_FULL = 2 * kORing, R_DONE = P_FULL + kNP, PV_DONE = R_DONE + kNP,
+              L_FULL = PV_DONE + kNP, O_FREE = L_FULL + 2, TOK_FULL_O, TOK_EMPTY_O = TOK_FULL_O + 2,
+              NBAR_O = TOK_EMPTY_O + 2 };
+constexpr int kNBar = 48;
+static_assert(NBAR_S <= kNBar && NBAR_O <= kNBar, "barrier slots");
+constexpr int SM_TMEM = SM_BAR + 8 * kNBar;
 constexpr int SM_SMID = SM_TMEM + 4;
 constexpr int SM_ABORT = SM_SMID + 4;
-constexpr int kSmemBytes = SM_ABORT + 4 + 1024;     // + alignment slack
+constexpr int kSmemBytes = SM_ABORT + 4 + 1024;          // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the exchange scratch is indexed by SM");
+static_assert(kSmemBytes > 232448 / 2, "one CTA per SM");
+static_assert(SM_STG % 1024 == 0 && SM_P % 1024 == 0 && kPBufStride % 1024 == 0 && kChunkKV % 1024 == 0, "swizzle atoms");
+static_assert(kPXBytes % 16 == 0 && kPXBytes <= kPBufStride, "bulk copy size");
+static_assert(kSUnitCh * kSUnits == 9 && kOUnitCh * kOUnits == 8, "units cover the rows");
 
+// every accumulator and every tcgen05.ld starts at a column that is a multiple of its width
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_O = 0;            // O: 256 columns
-constexpr uint32_t TM_S = 256;          // partial then full scores of one block: 64 columns
-constexpr uint32_t TM_Q = 320;          // this CTA's q slice, bf16 pairs: 128 | 160 columns
-static_assert(SM_P % 1024 == 0, "swizzle atoms");
+constexpr uint32_t TM_S = 0;            // score CTA: two 64-column score buffers (buffer g for group g)
+constexpr uint32_t TM_Q = 128;          // score CTA: q as bf16 pairs, 288 columns
+constexpr uint32_t TM_O = 0;            // output CTA: O, 512 columns
 
 struct TcFwdParams {
   const uint16_t* q;                    // [T, H, 576] bf16
   const uint16_t* kv;                   // [T, 576] bf16
-  float* xchg;                          // exchange scratch, kXchgSlots slots
   const int32_t* indices;
   uint16_t* out;
   float* lse;
   uint32_t* status;
   int T, H, topk;                       // H <= 128 heads; rows H..127 of the tile are zero
-  int t0;                               // this launch handles query rows t0, t0 + 1, ...
+  int t0, nt;                           // this launch handles query rows [t0, t0 + nt)
   float c2;                             // scale * log2(e)
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
-// kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+// bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
+// another CTA's (addresses from mapa); completes tx on the destination's barrier
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+#ifdef SMLA_TRACE
+#define SMLA_TRACE_ARGS , long long trace_t0, int trace_cta
+#define SMLA_TRACE_PASS , trace_t0, trace_cta
+#else
+#define SMLA_TRACE_ARGS
+#define SMLA_TRACE_PASS
+#endif
+constexpr int kTraceGb0 = 100;          // trace rows: global blocks kTraceGb0 .. kTraceGb0 + 32
+
+// Number of tokens of this cluster (tokens cl, cl + ncl, ... of the launch).
+__device__ __forceinline__ int cluster_tokens(const TcFwdParams& p, int cl, int ncl) {
+  return cl < p.nt ? (p.nt - 1 - cl) / ncl + 1 : 0;
+}
+
+// Producer warps: for each token of the cluster, list the blocks that hold a
+// valid slot, publish the token's block count to the other roles, then
+// gather the rows unit by unit into the ring of NRING units of UCH chunks
+// (UPB units per block).  With kMask the slot-validity mask of each block is
+// written into the mask ring for the softmax.
+template <int UCH, int UPB, int NRING, bool kMask>
+__device__ __forceinline__ void produce(const TcFwdParams& p, uint32_t sb, uint8_t* smem, int cl, int ncl,
+                                        volatile int* abort_flag, int full0, int empty0, int tokfull0,
+                                        int tokempty0 SMLA_TRACE_ARGS) {
+  const int pt = threadIdx.x;              // 0..127
+  const int warp = pt >> 5, lane = pt & 31;
+  const int c16 = pt & 7, r0 = pt >> 3;    // 16-byte piece c16 of rows r0 + 16 j of every chunk
+  constexpr int RS = kProducers / 8;
+  constexpr int kUnitBytes = UCH * kChunkKV;
+  const int nblk = p.topk / kBK;
+  const int ntok = cluster_tokens(p, cl, ncl);
+  uint8_t* flag = smem + SM_BFLAG;
+  int16_t* blist = reinterpret_cast<int16_t*>(smem + SM_BLIST);
+  volatile int* nbs = reinterpret_cast<volatile int*>(smem + SM_NB);
+  volatile int* tok = reinterpret_cast<volatile int*>(smem + SM_TOK);
+  const uint16_t* kvc = p.kv + 8 * c16;
+  int n = 0, gb = 0;                       // units and blocks gathered so far (all tokens)
+  for (int k = 0; k < ntok; ++k) {
+    const int t = p.t0 + cl + k * ncl;
+    const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    // the blocks of this token that hold a valid slot (0 <= idx < T)
+    for (int b = pt; b < nblk; b += kProducers) {
+      const int4* ib = reinterpret_cast<const int4*>(irow + b * kBK);
+      bool v = false;
+#pragma unroll 4
+      for (int c = 0; c < kBK / 4; ++c) {
+        const int4 x = __ldg(ib + c);
+        v |= (x.x >= 0 && x.x < p.T) | (x.y >= 0 && x.y < p.T) | (x.z >= 0 && x.z < p.T) | (x.w >= 0 && x.w < p.T);
+      }
+      flag[b] = v ? 1 : 0;
+    }
+    named_bar_sync(kProdBar, kProducers);
+    if (warp == 0) {
+      int base = 0;
+      for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const bool f = (b0 + lane < nblk) && flag[b0 + lane];
+        const uint32_t m = __ballot_sync(0xffffffffu, f);
+        if (f) blist[base + __popc(m & ((1u << lane) - 1u))] = (int16_t)(b0 + lane);
+        base += __popc(m);
+      }
+      // publish the token's block count (the slot of token k - 2 must have been read)
+      const bool ok = k < 2 || __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, tokempty0 + (k & 1)), ((k >> 1) - 1) & 1,
+                                                                 abort_flag, p.status));
+      if (lane == 0) {
+        *nbs = ok ? base : -1;
+        if (ok) {
+          tok[k & 1] = base;
+          mbar_arrive(bar_addr(sb, tokfull0 + (k & 1)));
+        }
+      }
+    }
+    named_bar_sync(kProdBar, kProducers);
+    const int nb = *nbs;
+    if (nb < 0) return;                    // uniform over the producer warps
+    int nxt[kRowsPerProducer], nm[2] = {0, 0};
+    if (nb > 0) {
+      const int32_t* ib = irow + blist[0] * kBK;
+#pragma unroll
+      for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+      if (kMask && warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
+    }
+    bool ok = true;
+    for (int i = 0; ok && i < nb; ++i, ++gb) {
+      int cur[kRowsPerProducer], cm[2];
+#pragma unroll
+      for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
+      cm[0] = nm[0]; cm[1] = nm[1];
+      if (i + 1 < nb) {                    // indices of the next block, one block ahead
+        const int32_t* ib = irow + blist[i + 1] * kBK;
+#pragma unroll
+        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
+        if (kMask && warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
+      }
+      const uint16_t* src[kRowsPerProducer];
+      uint32_t dsto[kRowsPerProducer], nbytes[kRowsPerProducer];
+#pragma unroll
+      for (int j = 0; j < kRowsPerProducer; ++j) {
+        const int r = r0 + RS * j;
+        const bool v = cur[j] >= 0 && cur[j] < p.T;
+        src[j] = kvc + (int64_t)(v ? cur[j] : 0) * kDqk;
+        dsto[j] = r * 128 + ((c16 ^ (r & 7)) << 4);
+        nbytes[j] = v ? 16u : 0u;
+      }
+      if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 9);
+#pragma unroll 1
+      for (int u = 0; u < UPB; ++u, ++n) {
+        const int slot = n % NRING;
+        if (n >= NRING &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, empty0 + slot), ((n / NRING) - 1) & 1, abort_flag,
+                                                     p.status))))
+          break;                           // warp-uniform exit
+        const uint32_t unit = sb + slot * kUnitBytes;
+#pragma unroll
+        for (int j = 0; j < kRowsPerProducer; ++j)
+#pragma unroll
+          for (int c = 0; c < UCH; ++c) cp_async16(unit + dsto[j] + c * kChunkKV, src[j] + 64 * (u * UCH + c), nbytes[j]);
+        cp_async_arrive(bar_addr(sb, full0 + slot));
+      }
+      if (!ok) break;
+      if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 10);
+      if (kMask && warp == 0) {            // slot validity of the block for the softmax
+        const int mr = gb % kMaskRing;
+        if (gb >= kMaskRing &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, M_EMPTY + mr), ((gb / kMaskRing) - 1) & 1, abort_flag,
+                                                     p.status))))
+          break;
+        const uint32_t ma = __ballot_sync(0xffffffffu, cm[0] >= 0 && cm[0] < p.T);
+        const uint32_t mb = __ballot_sync(0xffffffffu, cm[1] >= 0 && cm[1] < p.T);
+        if (lane == 0) {
+          *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * mr) = (uint64_t)ma | ((uint64_t)mb << 32);
+          mbar_arrive(bar_addr(sb, M_FULL + mr));
+        }
+      }
+    }
+    if (!ok) return;
+  }
+}
+
+// Block count of the cluster's token k, from the token ring (one read per
+// calling thread, acknowledged on the ring's empty barrier).  -1 on abort.
+template <bool kWarp>
+__device__ __forceinline__ int read_token(const TcFwdParams& p, uint32_t sb, uint8_t* smem, int k, int tokfull0,
+                                          int tokempty0, volatile int* abort_flag) {
+  const bool ok = kWarp ? __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, tokfull0 + (k & 1)), (k >> 1) & 1, abort_flag,
+                                                            p.status))
+                        : mbar_wait(bar_addr(sb, tokfull0 + (k & 1)), (k >> 1) & 1, abort_flag, p.status);
+  if (!ok) return -1;
+  const int nb = reinterpret_cast<volatile int*>(smem + SM_TOK)[k & 1];
+  mbar_arrive(bar_addr(sb, tokempty0 + (k & 1)));
+  return nb;
+}
+
+// kAllHeads: H == 128 (no zero rows)
 template <bool kAllHeads>
 __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     tc_fwd_h128_kernel(TcFwdParams p) {
@@ -105,33 +308,55 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned (128B swizzle atoms)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();          // 0 or 1
+  const uint32_t crank = cluster_ctarank();          // 0: score CTA, 1: output CTA
   const uint32_t peer = crank ^ 1u;
-  const int t = p.t0 + (blockIdx.x >> 1);
-  const int nch = 4 + (int)crank;                     // 64-dim key chunks of this CTA
-  const int g0 = 4 * (int)crank;                      // first global chunk
-  const int nblk = p.topk / kBK;           // blocks of the token's slot list
+  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int ntok = cluster_tokens(p, cl, ncl);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int k = 0; k < kStages; ++k) {
-      mbar_init(bar_addr(sb, KV_FULL + k), kProducers + 1);   // cp.async arrivals + the slot mask
-      mbar_init(bar_addr(sb, KV_EMPTY + k), 1);
+    if (crank == 0) {
+      for (int k = 0; k < kSRing; ++k) {
+        mbar_init(bar_addr(sb, KV_FULL + k), kProducers);      // cp.async arrivals
+        mbar_init(bar_addr(sb, KV_EMPTY + k), 1);              // the MMAs that read the unit completed
+      }
+      for (int k = 0; k < kMaskRing; ++k) {
+        mbar_init(bar_addr(sb, M_FULL + k), 1);
+        mbar_init(bar_addr(sb, M_EMPTY + k), 128);             // the softmax group read the mask
+      }
+      mbar_init(bar_addr(sb, Q_FULL), 256);                    // both groups stored their chunks of q
+      mbar_init(bar_addr(sb, Q_EMPTY), 1);                     // the token's score MMAs completed
+      for (int g = 0; g < 2; ++g) {
+        mbar_init(bar_addr(sb, S_FULL + g), 1);
+        mbar_init(bar_addr(sb, S_FREE + g), 128);
+        mbar_init(bar_addr(sb, ST_FULL + g), 128);    // group g wrote the running state after its block
+        mbar_init(bar_addr(sb, L_EMPTY + g), 128);    // the output CTA read a token's final sums
+        mbar_init(bar_addr(sb, TOK_FULL_S + g), 1);
+        mbar_init(bar_addr(sb, TOK_EMPTY_S + g), 1 + 1 + 256);   // MMA, P mover, both softmax groups
+      }
+      for (int k = 0; k < kNS; ++k) {
+        mbar_init(bar_addr(sb, STG_FULL + k), 128);   // a group wrote P into staging buffer k
+        mbar_init(bar_addr(sb, STG_FREE + k), 1);     // the bulk copy has read it
+      }
+      for (int k = 0; k < kNP; ++k) mbar_init(bar_addr(sb, P_FREE + k), 1);   // the output CTA's P buffer k is free
+    } else {
+      for (int k = 0; k < kORing; ++k) {
+        mbar_init(bar_addr(sb, V_FULL + k), kProducers);
+        mbar_init(bar_addr(sb, V_EMPTY + k), 1);
+      }
+      for (int k = 0; k < kNP; ++k) {
+        mbar_init(bar_addr(sb, P_FULL + k), 1);       // armed with expect_tx; the bulk copy completes it
+        mbar_init(bar_addr(sb, R_DONE + k), 128);     // rows rescaled where the max moved
+        mbar_init(bar_addr(sb, PV_DONE + k), 1);
+      }
+      for (int g = 0; g < 2; ++g) {
+        mbar_init(bar_addr(sb, L_FULL + g), 128);
+        mbar_init(bar_addr(sb, TOK_FULL_O + g), 1);
+        mbar_init(bar_addr(sb, TOK_EMPTY_O + g), 1 + 1 + 128);   // MMA, P keeper, rows
+      }
+      mbar_init(bar_addr(sb, O_FREE), 128);           // the epilogue read O out of TMEM
     }
-    mbar_init(bar_addr(sb, Q_FULL), 256);       // both groups stored their part of q into TMEM
-    mbar_init(bar_addr(sb, S_FULL + 0), 1);
-    mbar_init(bar_addr(sb, S_FULL + 1), 1);
-    mbar_init(bar_addr(sb, S_FREE), 128);       // a group loaded the partial scores into registers
-    mbar_init(bar_addr(sb, ST_FULL + 0), 128);  // the group wrote the running state after its block
-    mbar_init(bar_addr(sb, ST_FULL + 1), 128);
-    mbar_init(bar_addr(sb, X_FULL + 0), 128);   // the peer's 128 threads wrote their partial rows
-    mbar_init(bar_addr(sb, X_FULL + 1), 128);
-    mbar_init(bar_addr(sb, X_EMPTY + 0), 128);  // the peer's 128 threads read ours
-    mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
-    mbar_init(bar_addr(sb, P_FULL), 128);
-    mbar_init(bar_addr(sb, O_DONE + 0), 1);
-    mbar_init(bar_addr(sb, O_DONE + 1), 1);
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -143,292 +368,366 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   __syncthreads();
   cluster_sync();   // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
+  SMLA_TRACE_T0;
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
-  // blocks that hold only padding contribute nothing and are skipped: list the
-  // others in order (both CTAs of the pair read the same indices and agree)
-  const int16_t* blist = reinterpret_cast<const int16_t*>(smem + SM_BLIST);
-  const int nb = build_block_list<kBK>(p.indices + (int64_t)t * p.topk, nblk, p.T, smem + SM_BFLAG,
-                                  reinterpret_cast<int16_t*>(smem + SM_BLIST), reinterpret_cast<int*>(smem + SM_NB));
 
-  if (warp < kProducers / 32) {
-    // ------------------------------------------------------------ producers
-    const int pt = threadIdx.x;              // 0..63
-    // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
-    const int c16 = pt & 7, r0 = pt >> 3;
-    constexpr int RS = kProducers / 8;       // row stride between a thread's rows
-    const int32_t* irow = p.indices + (int64_t)t * p.topk;
-    const uint16_t* kvc = p.kv + 64 * g0 + 8 * c16;
-    int nxt[kRowsPerProducer], nm[2];
-    if (nb > 0) {
-      const int32_t* ib = irow + blist[0] * kBK;
-#pragma unroll
-      for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
-      if (warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
-    }
-    for (int i = 0; i < nb; ++i) {
-      const int st = i % kStages, use = i / kStages;
-      int cur[kRowsPerProducer], cm[2];
-#pragma unroll
-      for (int j = 0; j < kRowsPerProducer; ++j) cur[j] = nxt[j];
-      cm[0] = nm[0]; cm[1] = nm[1];
-      if (i + 1 < nb) {                      // indices of the next block, one block ahead
-        const int32_t* ib = irow + blist[i + 1] * kBK;
-#pragma unroll
-        for (int j = 0; j < kRowsPerProducer; ++j) nxt[j] = __ldg(ib + r0 + RS * j);
-        if (warp == 0) { nm[0] = __ldg(ib + lane); nm[1] = __ldg(ib + 32 + lane); }
-      }
-      if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + st), (use - 1) & 1, abort_flag,
-                                                        p.status)))
-        break;                                 // warp-uniform exit
-      const uint32_t stage = sb + SM_KV + st * kStageBytes;
-#pragma unroll
-      for (int j = 0; j < kRowsPerProducer; ++j) {
-        const int r = r0 + RS * j;
-        const bool v = cur[j] >= 0 && cur[j] < p.T;
-        const uint16_t* src = kvc + (int64_t)(v ? cur[j] : 0) * kDqk;
-        const uint32_t dst = stage + r * 128 + ((c16 ^ (r & 7)) << 4);
-        for (int k = 0; k < nch; ++k) cp_async16(dst + k * kChunkKV, src + 64 * k, v ? 16u : 0u);
-      }
-      cp_async_arrive(bar_addr(sb, KV_FULL + st));
-      if (warp == 0) {                        // slot validity mask of the block for the softmax warps
-        const uint32_t ma = __ballot_sync(0xffffffffu, cm[0] >= 0 && cm[0] < p.T);
-        const uint32_t mb = __ballot_sync(0xffffffffu, cm[1] >= 0 && cm[1] < p.T);
-        if (lane == 0) {
-          *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st) = (uint64_t)ma | ((uint64_t)mb << 32);
-          mbar_arrive(bar_addr(sb, KV_FULL + st));
-        }
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Event driven: the score MMAs of block i are issued as soon as its KV stage
-    // has landed and its TMEM score buffer is free, the PV MMA of block j as soon
-    // as P(j) is written, whichever comes first.
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
-      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
-      // base descriptors; per-MMA descriptors only move the start address
-      const uint64_t dk0 = sdesc_sw128(sb + SM_KV, 16, 1024);
-      const uint64_t dp0 = sdesc_sw128(sb + SM_P, 16, 1024);
-      // V is the first four chunks of the stage, read MN-major:
-      // LBO = stride between 64-dim chunks, SBO = stride between 8-row groups
-      const uint64_t dv0 = sdesc_sw128(sb + SM_KV, kChunkKV, 1024);
-      bool ok = mbar_wait(bar_addr(sb, Q_FULL), 0, abort_flag, p.status);
-      tc_fence_after();
-      int ns = 0, npv = 0;                    // next block for the score MMAs / for PV
-      unsigned long long idle_since = 0;
-      while (ok && npv < nb) {
-        bool progress = false;
-        if (ns < nb) {
-          const int st = ns % kStages;
-          if (mbar_try_wait(bar_addr(sb, KV_FULL + st), (ns / kStages) & 1) &&
-              (ns < 1 || mbar_try_wait(bar_addr(sb, S_FREE), (ns - 1) & 1))) {
-            fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 5; ++k) {
-              if (k < nch) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  mma_bf16_ts(tmem + TM_S, tmem + TM_Q + 32 * k + 8 * ks,
-                              sdesc_add(dk0, st * kStageBytes + k * kChunkKV + ks * 32), idesc_s, (k | ks) != 0);
-              }
-            }
-            mma_commit(bar_addr(sb, S_FULL + (ns & 1)));
-            ++ns;
-            progress = true;
-          }
-        }
-        if (npv < ns && mbar_try_wait(bar_addr(sb, P_FULL), npv & 1)) {
-          const int stj = npv % kStages;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tmem + TM_O, sdesc_add(dp0, ks * 32), sdesc_add(dv0, stj * kStageBytes + ks * 16 * 128),
-                        idesc_pv, (npv > 0 || ks > 0));
-          mma_commit(bar_addr(sb, O_DONE + (npv & 1)));
-          mma_commit(bar_addr(sb, KV_EMPTY + stj));
-          ++npv;
-          progress = true;
-        }
-        if (progress) {
-          idle_since = 0;
-        } else if (*abort_flag) {
-          break;
-        } else {
-          const unsigned long long now = globaltimer();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (now - idle_since > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicCAS(p.status, 0u, kErrWaitTimeout);
-            break;
-          }
-        }
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ exchange + softmax
-    // Two groups of four warps take alternate blocks (group g: blocks i = g mod 2)
-    // so that one group's score exchange overlaps the other's softmax.  The
-    // running max and the two sums pass from group to group through shared
-    // memory, in block order.
-    const int g = (warp - kGroup0) >> 2;
-    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-    const int h = 32 * q4 + lane;            // head == TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    uint8_t* prow = smem + SM_P + h * 128;
-    volatile float* state = reinterpret_cast<volatile float*>(smem + SM_STATE) + 4 * h;
-    const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
-    const uint32_t xempty_peer = mapa(bar_addr(sb, X_EMPTY), peer);
-    // exchange slots of this CTA's SM and of the peer's SM
-    const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
-    const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
-    float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
-    // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
-    // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
-    float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
-    // this CTA's q slice into TMEM (the A operand of the score MMAs): head h in
-    // lane h, dims packed two per column; group g stores chunks g, g+2, ...
-    {
-      const bool real = h < p.H;             // heads past H are zero rows of the tile
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk + 64 * g0);
-      for (int k = g; k < nch; k += 2) {
-        uint4 v[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = real ? __ldg(qrow + 8 * k + c) : make_uint4(0u, 0u, 0u, 0u);
-        tmem_st32(tl + TM_Q + 32 * k, reinterpret_cast<const float*>(v));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, Q_FULL));
-    }
-    bool ok = true;
-    for (int i = g; i < nb; i += 2) {
-      const int b = g, st = i % kStages, k2 = i >> 1;
-      // own partial scores; the TMEM buffer is free again once they are in registers
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + b), k2 & 1, abort_flag, p.status)))) break;
-      tc_fence_after();
-      float s[64];
-      tmem_ld64(tl + TM_S, s);
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, S_FREE));
-      // publish them to the peer, then add the peer's
-      if (k2 >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_EMPTY + b), (k2 - 1) & 1, abort_flag,
-                                                                   p.status))))
-        break;
-      // rows past H (zero q rows: their partial scores are exactly 0 on both
-      // CTAs) skip the exchange; every thread still arrives
-      const bool xreal = kAllHeads || h < p.H;
-      float4* wr = xmine + b * (kXchgBufFloats / 4);
-      if (xreal) {
-#pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) wr[v4 * 128] = make_float4(s[4 * v4], s[4 * v4 + 1], s[4 * v4 + 2], s[4 * v4 + 3]);
-      }
-      mbar_arrive_remote(xfull_peer + 8 * b);     // release: the rows are visible to the peer
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, X_FULL + b), k2 & 1, abort_flag, p.status))))
-        break;
-      const float4* rd = xpeer + b * (kXchgBufFloats / 4);
-      if (xreal) {
-#pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) {
-          const float4 o = ld_cg_v4(rd + v4 * 128);
-          s[4 * v4] += o.x; s[4 * v4 + 1] += o.y; s[4 * v4 + 2] += o.z; s[4 * v4 + 3] += o.w;
-        }
-      }
-      mbar_arrive_remote(xempty_peer + 8 * b);    // the peer may reuse that buffer
-      // slot validity of this block (written by the producer before it armed KV_FULL)
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i / kStages) & 1, abort_flag, p.status)))) break;
-      const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * st);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        s[j] = ((mask >> j) & 1ull) ? s[j] * p.c2 : -INFINITY;
-        mx = fmaxf(mx, s[j]);
-      }
-      // running state after block i-1, from the other group
-      if (i >= 1) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, ST_FULL + (g ^ 1)), ((i - 1) >> 1) & 1, abort_flag,
-                                                     p.status))))
-          break;
-        m_run = state[0]; l = state[1]; l_bf = state[2];
-      }
-      // lazily updated running max: move it only when the block max exceeds it by > 8 (log2 units)
-      const bool move = mx > m_run + kLazyRescale;
-      const float m_new = move ? mx : m_run;
-      const float alpha = move ? ex2(m_run - m_new) : 1.f;   // m_run = -inf gives 0
-      // while no valid slot has been seen m_new is -inf; subtract 0 instead so
-      // that padding gives exp2(-inf) = 0 and never exp2(-inf - -inf) = NaN
-      const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-      float sum = 0.f, sum_bf = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2(s[2 * j] - m_sub), p1 = ex2(s[2 * j + 1] - m_sub);   // -inf -> 0
-        sum += p0 + p1;
-        pk[j] = pack_bf16x2(p0, p1);
-        sum_bf += bf16_lo(pk[j]) + bf16_hi(pk[j]);    // the weights the PV MMA actually uses
-      }
-      l = l * alpha + sum;
-      l_bf = l_bf * alpha + sum_bf;
-      m_run = m_new;
-      state[0] = m_run; state[1] = l; state[2] = l_bf;
-      mbar_arrive(bar_addr(sb, ST_FULL + g));
-      // P buffer and O are free once the previous PV has completed
-      if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + (b ^ 1)), ((i - 1) >> 1) & 1, abort_flag,
-                                                             p.status))))
-        break;
-      tc_fence_after();
-      if (i >= 1 && __any_sync(0xffffffffu, move)) {
+  if (crank == 0) {
+    // ================================================================ score CTA
+    if (warp < kProducers / 32) {
+      produce<kSUnitCh, kSUnits, kSRing, true>(p, sb, smem, cl, ncl, abort_flag, KV_FULL, KV_EMPTY, TOK_FULL_S,
+                                               TOK_EMPTY_S SMLA_TRACE_PASS);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        // MMA issuer: S of each block into buffer gb & 1, unit by unit as the K units land
+        const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
+        const uint64_t dk0 = sdesc_sw128(sb + SM_K, 16, 1024);
+        int gb = 0, n = 0;
+        bool ok = true;
+        for (int k = 0; ok && k < ntok; ++k) {
+          const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
+          if (!(ok = nb >= 0)) break;
+          if (!(ok = mbar_wait(bar_addr(sb, Q_FULL), k & 1, abort_flag, p.status))) break;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int b = gb & 1;
+            if (gb >= 2 && !(ok = mbar_wait(bar_addr(sb, S_FREE + b), ((gb >> 1) - 1) & 1, abort_flag, p.status))) break;
+            SMLA_STAMP(gb - kTraceGb0, 0);
 #pragma unroll 1
-        for (int part = 0; part < 8; ++part) {
-          float o[32];
-          tmem_ld32(tl + TM_O + 32 * part, o);
+            for (int u = 0; u < kSUnits; ++u, ++n) {
+              const int slot = n % kSRing;
+              if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
+              fence_proxy_async_smem();   // cp.async wrote the unit through the generic proxy
+              tc_fence_after();
+              // S += q K^T over the unit's chunks (A = q from TMEM)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= alpha;
-          tmem_st32(tl + TM_O + 32 * part, o);
+              for (int c = 0; c < kSUnitCh; ++c)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                  const int kk = u * kSUnitCh + c;
+                  mma_bf16_ts(tmem + TM_S + 64 * b, tmem + TM_Q + 32 * kk + 8 * ks,
+                              sdesc_add(dk0, slot * kSUnitCh * kChunkKV + c * kChunkKV + ks * 32), idesc_s,
+                              (kk | ks) != 0);
+                }
+              mma_commit(bar_addr(sb, KV_EMPTY + slot));
+            }
+            if (!ok) break;
+            mma_commit(bar_addr(sb, S_FULL + b));
+            SMLA_STAMP(gb - kTraceGb0, 1);
+          }
+          if (ok) mma_commit(bar_addr(sb, Q_EMPTY));   // q's TMEM may take the next token once these complete
+        }
+      } else if (lane == 1) {
+        // P mover: one bulk copy per block from a staging buffer into the output CTA's P buffer
+        const uint32_t pbuf_peer = mapa(sb + SM_P, peer), pfull_peer = mapa(bar_addr(sb, P_FULL), peer);
+        int gb = 0;
+        bool ok = true;
+        for (int k = 0; ok && k < ntok; ++k) {
+          const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
+          if (!(ok = nb >= 0)) break;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int sg = gb % kNS, pb = gb % kNP;
+            if (!(ok = mbar_wait(bar_addr(sb, STG_FULL + sg), (gb / kNS) & 1, abort_flag, p.status))) break;
+            if (gb >= kNP &&
+                !(ok = mbar_wait<true>(bar_addr(sb, P_FREE + pb), ((gb / kNP) - 1) & 1, abort_flag, p.status)))
+              break;
+            SMLA_STAMP(gb - kTraceGb0, 11);
+            bulk_s2s(pbuf_peer + pb * kPBufStride, sb + SM_STG + sg * kPBufStride, kPXBytes, pfull_peer + 8 * pb);
+            bulk_commit();
+            if (gb >= 1) {                       // the copy before this one has read its staging buffer
+              bulk_wait_read<1>();
+              mbar_arrive(bar_addr(sb, STG_FREE + (gb - 1) % kNS));
+            }
+          }
+        }
+        bulk_wait_read<0>();                     // no copy still reads this CTA's shared memory
+        if (ok && gb > 0) mbar_arrive(bar_addr(sb, STG_FREE + (gb - 1) % kNS));
+      }
+      __syncwarp();
+    } else {
+      // two softmax groups, one thread per head each: group g takes the blocks whose
+      // running index is g mod 2; within a token the running max and sums pass from
+      // group to group through shared memory in block order
+      const int g = (warp - kRowWarp0) >> 2;
+      const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+      const int h = 32 * q4 + lane;
+      const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+      const bool real = kAllHeads || h < p.H;
+      volatile float* state = reinterpret_cast<volatile float*>(smem + SM_STATE) + 4 * h;
+      const uint32_t lbf_peer = mapa(sb + SM_LBF + 4 * h, peer), lfull_peer = mapa(bar_addr(sb, L_FULL), peer);
+      if (real && ntok > 0) {                  // the first token's q row into L2
+        const uint8_t* q0 = reinterpret_cast<const uint8_t*>(p.q + ((int64_t)(p.t0 + cl) * p.H + h) * kDqk);
+        for (int c = g; c < 9; c += 2) prefetch_l2(q0 + 128 * c);
+      }
+      int gb = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < ntok; ++k) {
+        const int t = p.t0 + cl + k * ncl;
+        const int nb = read_token<true>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
+        if (!(ok = nb >= 0)) break;
+        // this token's q into TMEM (the A operand of the score MMAs) once the previous
+        // token's score MMAs completed: group g stores chunks g, g + 2, ...
+        if (k >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, Q_EMPTY), (k - 1) & 1, abort_flag, p.status))))
+          break;
+        tc_fence_after();
+        {
+          const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk);
+          uint4 v[2][8];
+#pragma unroll
+          for (int c0 = 0; c0 < 10; c0 += 4) {     // two chunks of the group per round (loads in flight together)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int kc = g + c0 + 2 * r;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                v[r][c] = (real && kc < 9) ? __ldg(qrow + 8 * kc + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int kc = g + c0 + 2 * r;
+              if (kc < 9) tmem_st32(tl + TM_Q + 32 * kc, reinterpret_cast<const float*>(v[r]));
+            }
+          }
         }
         tmem_wait_st();
-      }
+        tc_fence_before();
+        mbar_arrive(bar_addr(sb, Q_FULL));
+        if (real && k + 1 < ntok) {            // the next token's q row into L2
+          const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q + ((int64_t)(t + ncl) * p.H + h) * kDqk);
+          for (int c = g; c < 9; c += 2) prefetch_l2(qn + 128 * c);
+        }
+        // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
+        // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
+        float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
+        const int gb0 = gb;
+        for (int j = (g - gb0) & 1; j < nb; j += 2) {
+          const int gbj = gb0 + j;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, S_FULL + g), (gbj >> 1) & 1, abort_flag, p.status))))
+            break;
+          tc_fence_after();
+          float s[64];
+          tmem_ld64(tl + TM_S + 64 * g, s);
+          tc_fence_before();
+          mbar_arrive(bar_addr(sb, S_FREE + g));
+          if (h == 0) SMLA_STAMP(gbj - kTraceGb0, 3);
+          // slot validity of this block
+          const int mr = gbj % kMaskRing;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, M_FULL + mr), (gbj / kMaskRing) & 1, abort_flag,
+                                                       p.status))))
+            break;
+          const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * mr);
+          mbar_arrive(bar_addr(sb, M_EMPTY + mr));
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) = v;
+          for (int jj = 0; jj < 64; ++jj) {
+            s[jj] = ((mask >> jj) & 1ull) ? s[jj] * p.c2 : -INFINITY;
+            mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
+          }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          // the running state after the token's previous block, from the other group; at
+          // a token's first block the state starts afresh, but the wait still orders this
+          // group's write of the shared state after the other group's last one
+          if (gbj >= 1 &&
+              !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, ST_FULL + (g ^ 1)), ((gbj - 1) >> 1) & 1,
+                                                       abort_flag, p.status))))
+            break;
+          if (j >= 1) {
+            m_run = state[0]; l = state[1]; l_bf = state[2];
+          } else {
+            m_run = -INFINITY; l = 0.f; l_bf = 0.f;
+          }
+          if (h == 0) SMLA_STAMP(gbj - kTraceGb0, 4);
+          float alpha = 1.f;
+          uint32_t pk[32];
+          if (real) {
+            // lazily updated running max: move it only when the block max exceeds it by > 8 (log2 units)
+            const bool move = mx > m_run + kLazyRescale;
+            const float m_new = move ? mx : m_run;
+            alpha = move ? ex2(m_run - m_new) : 1.f;   // m_run = -inf gives 0 (first block of a token: no O yet)
+            // a listed block has a valid slot, so m_new is finite; the guard keeps
+            // exp2(-inf - -inf) out regardless
+            const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f}, sbf4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const float p0 = ex2(s[2 * jj] - m_sub), p1 = ex2(s[2 * jj + 1] - m_sub);   // -inf -> 0
+              sum4[jj & 3] += p0 + p1;
+              pk[jj] = pack_bf16x2(p0, p1);
+              sbf4[jj & 3] += bf16_lo(pk[jj]) + bf16_hi(pk[jj]);   // the weights the PV MMA actually uses
+            }
+            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            l_bf = l_bf * alpha + ((sbf4[0] + sbf4[1]) + (sbf4[2] + sbf4[3]));
+            m_run = m_new;
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) pk[jj] = 0u;   // rows past H: P = 0, O stays 0
+          }
+          state[0] = m_run; state[1] = l; state[2] = l_bf;
+          mbar_arrive(bar_addr(sb, ST_FULL + g));
+          // P and alpha into a staging buffer (the P mover copies it to the output CTA)
+          const int sg = gbj % kNS;
+          if (gbj >= kNS && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, STG_FREE + sg), ((gbj / kNS) - 1) & 1,
+                                                                      abort_flag, p.status))))
+            break;
+          uint8_t* xb = smem + SM_STG + sg * kPBufStride;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(xb + h * 128 + ((c ^ (h & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          reinterpret_cast<float*>(xb + kPBytes)[h] = alpha;
+          fence_proxy_async_smem();                  // the bulk copy reads it through the async proxy
+          mbar_arrive(bar_addr(sb, STG_FULL + sg));
+          if (h == 0) SMLA_STAMP(gbj - kTraceGb0, 5);
+        }
+        if (!ok) break;
+        gb = gb0 + nb;
+        // the group that took the token's last block holds its final state
+        const bool last = (nb == 0) ? (g == 0) : (g == ((gb - 1) & 1));
+        if (last) {
+          if (k >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, L_EMPTY + (k & 1)), ((k >> 1) - 1) & 1,
+                                                                     abort_flag, p.status))))
+            break;
+          // the sum of rounded weights goes to the output CTA, the LSE to global memory
+          st_cluster_f32(lbf_peer + 512 * (k & 1), l_bf);
+          mbar_arrive_remote(lfull_peer + 8 * (k & 1));
+          if (real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
+        }
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, P_FULL));
     }
-    // the group that took the last block holds the final state and writes the outputs
-    const bool last = (nb == 0) ? (g == 0) : (g == ((nb - 1) & 1));
-    if (ok && last && nb > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, O_DONE + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1, abort_flag,
-                                             p.status));
-    tc_fence_after();
-    if (ok && last) {
-      const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
-      const bool real = h < p.H;
-      uint16_t* orow = p.out + ((int64_t)t * p.H + h) * kDv + 256 * crank;
+  } else {
+    // ================================================================ output CTA
+    if (warp < kProducers / 32) {
+      produce<kOUnitCh, kOUnits, kORing, false>(p, sb, smem, cl, ncl, abort_flag, V_FULL, V_EMPTY, TOK_FULL_O,
+                                                TOK_EMPTY_O SMLA_TRACE_PASS);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        // MMA issuer: O += P V once a block's rows are rescaled, one N = 256 tile per V unit
+        const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+        const uint64_t dp0 = sdesc_sw128(sb + SM_P, 16, 1024);
+        // V read MN-major from the unit: LBO = stride between 64-dim chunks, SBO = 8-row groups
+        const uint64_t dv0 = sdesc_sw128(sb + SM_V, kChunkKV, 1024);
+        int gb = 0, n = 0;
+        bool ok = true;
+        for (int k = 0; ok && k < ntok; ++k) {
+          const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_O, TOK_EMPTY_O, abort_flag);
+          if (!(ok = nb >= 0)) break;
+          // O is free once the previous token's epilogue has read it
+          if (k >= 1 && nb > 0 && !(ok = mbar_wait(bar_addr(sb, O_FREE), (k - 1) & 1, abort_flag, p.status))) break;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int pb = gb % kNP;
+            if (!(ok = mbar_wait(bar_addr(sb, R_DONE + pb), (gb / kNP) & 1, abort_flag, p.status))) break;
+            SMLA_STAMP(gb - kTraceGb0, 7);
 #pragma unroll 1
-      for (int part = 0; part < 8; ++part) {
-        float o[32];
-        if (nb > 0) {
-          tmem_ld32(tl + TM_O + 32 * part, o);
-        } else {                             // no valid slot: no PV ever wrote O
+            for (int u = 0; u < kOUnits; ++u, ++n) {
+              const int slot = n % kORing;
+              if (!(ok = mbar_wait(bar_addr(sb, V_FULL + slot), (n / kORing) & 1, abort_flag, p.status))) break;
+              fence_proxy_async_smem();
+              tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+              for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + TM_O + 256 * u, sdesc_add(dp0, pb * kPBufStride + ks * 32),
+                            sdesc_add(dv0, slot * kOUnitCh * kChunkKV + ks * 16 * 128), idesc_pv, (j > 0 || ks > 0));
+              mma_commit(bar_addr(sb, V_EMPTY + slot));
+            }
+            if (!ok) break;
+            mma_commit(bar_addr(sb, PV_DONE + pb));
+            SMLA_STAMP(gb - kTraceGb0, 8);
+          }
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * part);
-        if (real) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+      } else if (lane == 1) {
+        // P buffer keeper: arms each buffer for its next block's bulk copy and tells the
+        // score CTA when PV has finished reading it
+        const uint32_t pfree_peer = mapa(bar_addr(sb, P_FREE), peer);
+        for (int b = 0; b < kNP; ++b) mbar_arrive_expect_tx(bar_addr(sb, P_FULL + b), kPXBytes);
+        int gb = 0;
+        bool ok = true;
+        for (int k = 0; ok && k < ntok; ++k) {
+          const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_O, TOK_EMPTY_O, abort_flag);
+          if (!(ok = nb >= 0)) break;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int pb = gb % kNP;
+            if (!(ok = mbar_wait(bar_addr(sb, PV_DONE + pb), (gb / kNP) & 1, abort_flag, p.status))) break;
+            mbar_arrive_expect_tx(bar_addr(sb, P_FULL + pb), kPXBytes);   // for block gb + kNP
+            mbar_arrive_remote(pfree_peer + 8 * pb);
+          }
         }
       }
-      if (crank == 0 && real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
+      __syncwarp();
+    } else if (warp < kRowWarp0 + 4) {
+      // one thread per head: rescale O when the max moved, then each token's epilogue
+      const int q4 = warp & 3;
+      const int h = 32 * q4 + lane;
+      const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+      const bool real = kAllHeads || h < p.H;
+      const uint32_t lempty_peer = mapa(bar_addr(sb, L_EMPTY), peer);
+      int gb = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < ntok; ++k) {
+        const int t = p.t0 + cl + k * ncl;
+        const int nb = read_token<true>(p, sb, smem, k, TOK_FULL_O, TOK_EMPTY_O, abort_flag);
+        if (!(ok = nb >= 0)) break;
+        for (int j = 0; ok && j < nb; ++j, ++gb) {
+          const int pb = gb % kNP;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, P_FULL + pb), (gb / kNP) & 1, abort_flag, p.status))))
+            break;
+          const float alpha = reinterpret_cast<volatile float*>(smem + SM_P + pb * kPBufStride + kPBytes)[h];
+          // the running max of this head moved: O (after the previous block's PV) is scaled by alpha
+          const bool resc = j >= 1 && alpha != 1.f;
+          if (__any_sync(0xffffffffu, resc)) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PV_DONE + (gb - 1) % kNP), ((gb - 1) / kNP) & 1,
+                                                         abort_flag, p.status))))
+              break;
+            tc_fence_after();
+            // tcgen05.ld / st are warp-collective: every lane takes part, lanes whose
+            // max did not move scale by exactly 1
+            const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+            for (int part = 0; part < 8; ++part) {
+              float o[64];
+              tmem_ld64(tl + TM_O + 64 * part, o);
+#pragma unroll
+              for (int jj = 0; jj < 64; ++jj) o[jj] *= f;
+              tmem_st64(tl + TM_O + 64 * part, o);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(bar_addr(sb, R_DONE + pb));
+        }
+        if (!ok) break;
+        // epilogue of the token: the final sums, then O once its last PV completed
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, L_FULL + (k & 1)), (k >> 1) & 1, abort_flag,
+                                                           p.status))))
+          break;
+        const float l_bf = reinterpret_cast<volatile float*>(smem + SM_LBF + 512 * (k & 1))[h];
+        mbar_arrive_remote(lempty_peer + 8 * (k & 1));
+        if (nb > 0 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PV_DONE + (gb - 1) % kNP), ((gb - 1) / kNP) & 1,
+                                                     abort_flag, p.status))))
+          break;
+        tc_fence_after();
+        const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
+        uint16_t* orow = p.out + ((int64_t)t * p.H + (real ? h : 0)) * kDv;
+        // every lane of the warp takes part in the warp-collective tcgen05.ld; only
+        // the rows of real heads are stored
+#pragma unroll 1
+        for (int part = 0; part < 8; ++part) {
+          float o[64];
+          if (nb > 0) {
+            tmem_ld64(tl + TM_O + 64 * part, o);
+          } else {                             // no valid slot: no PV ever wrote O
+#pragma unroll
+            for (int c = 0; c < 64; ++c) o[c] = 0.f;
+          }
+          if (real) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 64 * part);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                  pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_addr(sb, O_FREE));     // the next token's PV may overwrite O
+      }
     }
   }
 
@@ -436,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   if (*abort_flag) __nanosleep(1000000);   // let copies and MMAs already issued land
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // the peer no longer touches this CTA's shared memory
+  cluster_sync();   // the peer no longer touches this CTA's shared memory or barriers
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -444,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
 }
 
 __device__ uint32_t g_status = 0;
+
 
 // Failure-detection self-test: one thread waits, through the same bounded
 // wait the tensor-core kernels use, on an mbarrier that nothing arrives on.
@@ -500,16 +800,31 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(all ? tc_fwd_h128_kernel<true> : tc_fwd_h128_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  float* xchg = tc_xchg_ptr();
-  if (!xchg) return cudaErrorInvalidSymbol;
   const int nt = a.nt < 0 ? a.T : a.nt;
   if (nt == 0) return cudaSuccess;
-  TcFwdParams p{a.q, a.kv, xchg, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.t0, a.scale * kLog2e};
+  int dev = 0, nsm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // persistent: one cluster per pair of SMs, each walking a strided list of tokens
+  const int nclusters = nt < nsm / 2 ? nt : nsm / 2;
+  TcFwdParams p{a.q, a.kv, a.indices, a.out, a.lse, status, a.T, a.H, a.topk, a.t0, nt, a.scale * kLog2e};
   if (all)
-    tc_fwd_h128_kernel<true><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
+    tc_fwd_h128_kernel<true><<<dim3(2 * nclusters), dim3(kThreads), kSmemBytes, s>>>(p);
   else
-    tc_fwd_h128_kernel<false><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(p);
+    tc_fwd_h128_kernel<false><<<dim3(2 * nclusters), dim3(kThreads), kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_setup(int tok0) {
+  static const long long z[tc::kTraceCtas * tc::kTracePerCta] = {};
+  if (cudaMemcpyToSymbol(tc::g_trace, z, sizeof(z)) != cudaSuccess) return -1;
+  return cudaMemcpyToSymbol(tc::g_trace_tok0, &tok0, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int smla_trace_read(long long* dst) {
+  return cudaMemcpyFromSymbol(dst, tc::g_trace, sizeof(long long) * tc::kTraceCtas * tc::kTracePerCta) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 }  // namespace smla
