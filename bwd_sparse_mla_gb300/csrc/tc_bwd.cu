@@ -43,10 +43,11 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 32;
-constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax + drain, w7..10 exchange + drain
+constexpr int kProducers = 64;          // w0..1 gather, w2 MMA, w3..6 softmax, w7..10 exchange, w11..14 dKV drain
 constexpr int kMmaWarp = 2;
 constexpr int kXchgWarp0 = 7;
-constexpr int kThreads = 352;
+constexpr int kDrainWarp0 = 11;
+constexpr int kThreads = 480;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4
 constexpr int kChunk = 128 * 128;       // 64-dim chunk of q / dO for 128 heads
 constexpr int kChunkKV = kBK * 128;     // 64-dim chunk of a 32-row KV block
@@ -146,9 +147,10 @@ __device__ __forceinline__ bool drain_any(uint32_t sb, uint32_t tl, uint32_t tm_
              : drain_cols<C0, NC, false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status);
 }
 
-// slot columns of each block drained by the exchange warps ([0, kXchgCols)) and by
-// the softmax warps (the rest): the exchange warps' other work per block is lighter
-constexpr int kXchgCols = 20;
+// slot columns of each block's dKV tiles drained by the drain warps ([0, kDrainCols))
+// and by the exchange warps (the rest)
+constexpr int kDrainCols = 32;
+constexpr int kXchgDrainCols = kBK - kDrainCols;
 
 // kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
 template <bool kAllHeads>
@@ -176,8 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     *abort_flag = 0;
     mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + mask/rows
     mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
-    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 256);   // MMA commit + softmax and exchange threads (mask / rows read)
-    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 256);
+    // MMA commit + softmax and exchange threads (mask / rows read) + drain threads (rows read)
+    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 256 + 128);
+    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 256 + 128);
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FREE), 256);      // both warp sets loaded the partial S / dP
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DKV_FULL), 1);
-    mbar_init(bar_addr(sb, DKV_FREE), 256);      // both warp sets loaded their half of the tiles
+    mbar_init(bar_addr(sb, DKV_FREE), kXchgDrainCols > 0 ? 256 : 128);   // the draining warp sets loaded their columns
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   __syncthreads();
   cluster_sync();
   tc_fence_after();
+  SMLA_TRACE_T0;
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
   // fewer than 128 heads: rows H..127 of every q / dO chunk are zero (the
   // MMAs read all 128 rows); the fence orders these stores before the MMAs
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         if (i < nb) {
           const int st = i & 1;
           if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status))) break;
+          SMLA_STAMP(i, 0);
           if (i >= 1 && !(ok = mbar_wait(bar_addr(sb, SDP_FREE), (i - 1) & 1, abort_flag, p.status))) break;
           fence_proxy_async_smem();   // cp.async wrote the stage through the generic proxy
           tc_fence_after();
@@ -327,10 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
               mma_bf16_ss(tmem + TM_DP, sdesc_add(ddo0, k * kChunk + ks * 32),
                           sdesc_add(dk0, st * kStage + k * kChunkKV + ks * 32), id_sdp, (k | ks) != 0);
           mma_commit(bar_addr(sb, SDP_FULL));
+          SMLA_STAMP(i, 1);
         }
         if (i >= 1) {
           const int j = i - 1, stj = j & 1;
           if (!(ok = mbar_wait(bar_addr(sb, P_FULL), j & 1, abort_flag, p.status))) break;
+          SMLA_STAMP(j, 2);
           tc_fence_after();
           // dQ_half += (hi + lo) K_half: A = dS' (K-major, 64B swizzle), B = K block read MN-major
 #pragma unroll
@@ -347,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
           //   dKV^T = q_half^T dS' + dO_half^T P   (A MN-major 128B swizzle, B MN-major 64B swizzle)
           if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE), (j - 1) & 1, abort_flag, p.status))) break;
+          SMLA_STAMP(j, 3);
           tc_fence_after();
           for (int m = 0; m < ntile; ++m) {
             const uint32_t d_t = tmem + TM_DKV + 64 * m;
@@ -366,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           mma_commit(bar_addr(sb, DKV_FULL));
           mma_commit(bar_addr(sb, PDS_FREE));
           mma_commit(bar_addr(sb, KV_EMPTY + stj));
+          SMLA_STAMP(j, 4);
         }
       }
     }
@@ -387,11 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const uint32_t peer_sm = ld_cluster_u32(mapa(sb + SM_SMID, peer));
     const float4* xpeer = reinterpret_cast<const float4*>(p.xchg + (size_t)(peer_sm % kXchgSlots) * kXchgSlotFloats) + h;
     bool ok = true;
-    int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
       const int st = i & 1, xb = i & 1;
       // own partial rows; the TMEM buffer is free once both warp sets hold them
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, SDP_FULL), i & 1, abort_flag, p.status)))) break;
+      if (h == 0) SMLA_STAMP(i, 5);
       tc_fence_after();
       float s[32], dp[32];
       tmem_ld32(tl + TM_S, s);
@@ -412,46 +421,39 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         }
       }
       mbar_arrive_remote(xempty_peer + 8 * xb);       // the peer may reuse that buffer
+      if (h == 0) SMLA_STAMP(i, 6);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(smem + SM_MASK + 4 * st);
-      const int rows = reinterpret_cast<const int*>(smem + SM_ROWS)[st * 32 + lane];
       mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      uint32_t pp[16], dd[16], dl2[16], pl[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
-        const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
-        const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
-        pp[j] = pack_bf16x2(p0, p1);
-        pl[j] = pack_bf16x2(p0 - bf16_lo(pp[j]), p1 - bf16_hi(pp[j]));
-        const float d0 = p.scale * p0 * (dp[2 * j] - dl), d1 = p.scale * p1 * (dp[2 * j + 1] - dl);
-        dd[j] = pack_bf16x2(d0, d1);
-        dl2[j] = pack_bf16x2(d0 - bf16_lo(dd[j]), d1 - bf16_hi(dd[j]));   // the part bf16 dropped
-      }
       // P / dS' buffers are free once this CTA's dQ / dKV MMAs of the previous block completed
       if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status))))
         break;
+      // P and dS' as bf16 pairs hi + lo, 8 slots (one 16-byte chunk of each half-row) at a time
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
-        *reinterpret_cast<uint4*>(prow + (((c + 4) ^ sw) << 4)) =
-            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dsrow + (((c + 4) ^ sw) << 4)) =
-            make_uint4(dl2[4 * c], dl2[4 * c + 1], dl2[4 * c + 2], dl2[4 * c + 3]);
+        uint32_t pp[4], dd[4], dl2[4], pl[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * c + jj;
+          const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
+          const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
+          const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
+          pp[jj] = pack_bf16x2(p0, p1);
+          pl[jj] = pack_bf16x2(p0 - bf16_lo(pp[jj]), p1 - bf16_hi(pp[jj]));
+          const float d0 = p.scale * p0 * (dp[2 * j] - dl), d1 = p.scale * p1 * (dp[2 * j + 1] - dl);
+          dd[jj] = pack_bf16x2(d0, d1);
+          dl2[jj] = pack_bf16x2(d0 - bf16_lo(dd[jj]), d1 - bf16_hi(dd[jj]));   // the part bf16 dropped
+        }
+        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+        *reinterpret_cast<uint4*>(prow + (((c + 4) ^ sw) << 4)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        *reinterpret_cast<uint4*>(dsrow + ((c ^ sw) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        *reinterpret_cast<uint4*>(dsrow + (((c + 4) ^ sw) << 4)) = make_uint4(dl2[0], dl2[1], dl2[2], dl2[3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_addr(sb, P_FULL));
-      // the softmax warps' columns of the previous block's dKV tiles
-      if (i >= 1 && !(ok = drain_any<kXchgCols, kBK - kXchgCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, h,
-                                                                 p.dkv32, gslot(i - 1), abort_flag, p.status)))
-        break;
-      prev_rows = rows;
+      if (h == 0) SMLA_STAMP(i, 7);
     }
-    if (ok && nb > 0)
-      ok = drain_any<kXchgCols, kBK - kXchgCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, h, p.dkv32,
-                                                 gslot(nb - 1), abort_flag, p.status);
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (nb - 1) & 1, abort_flag, p.status));
     tc_fence_after();
@@ -475,11 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ exchange + dKV drain
+  } else if (warp < kDrainWarp0) {
+    // ------------------------------------------------------------ exchange
     // Publishes this CTA's partial S / dP rows of each block to its L2 exchange
-    // slot (the peer's softmax warps read them), then drains the first half of
-    // the previous block's dKV tiles.
+    // slot (the peer's softmax warps read them), then drains its share of the
+    // previous block's dKV tiles (slot columns kDrainCols..31).
     const int q4 = warp & 3;
     const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
@@ -513,20 +515,52 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         }
       }
       mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
-      // row list of block i (the softmax warps read it too), then the exchange
-      // warps' columns of the previous block's dKV tiles
+      if (L == 0) SMLA_STAMP(i, 9);
+      // row list of block i (the mask for the softmax warps is in the same stage)
       const int st = i & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
       const int rows = srows[st * 32 + lane];
       mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      if (i >= 1 && !(ok = drain_any<0, kXchgCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, L, p.dkv32,
-                                                   gslot(i - 1), abort_flag, p.status)))
-        break;
+      if constexpr (kXchgDrainCols > 0) {
+        if (i >= 1 && !(ok = drain_any<kDrainCols, kXchgDrainCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, L,
+                                                                   p.dkv32, gslot(i - 1), abort_flag, p.status)))
+          break;
+      }
       prev_rows = rows;
     }
-    if (ok && nb > 0)
-      drain_any<0, kXchgCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, L, p.dkv32, gslot(nb - 1), abort_flag,
-                              p.status);
+    if constexpr (kXchgDrainCols > 0) {
+      if (ok && nb > 0)
+        drain_any<kDrainCols, kXchgDrainCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, L, p.dkv32,
+                                              gslot(nb - 1), abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ dKV drain
+    // Reads each block's dKV^T tiles from TMEM once the MMAs have written them and
+    // adds them into the fp32 rows the block's valid slots name (slot columns
+    // 0..kDrainCols-1).  A block's row list is read from its KV stage as soon as the
+    // stage lands, one block ahead, so the stage is not held back.
+    const int q4 = warp & 3;
+    const int L = 32 * q4 + lane;               // TMEM lane: dim within a tile
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
+    bool ok = true;
+    auto read_rows = [&](int j, int& out) -> bool {
+      const int st = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (j >> 1) & 1, abort_flag, p.status))) return false;
+      out = srows[st * 32 + lane];
+      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
+      return true;
+    };
+    int rows = -1, nxt = -1;
+    if (nb > 0) ok = read_rows(0, rows);
+    for (int j = 0; ok && j < nb; ++j) {
+      if (j + 1 < nb && !(ok = read_rows(j + 1, nxt))) break;
+      if (!(ok = drain_any<0, kDrainCols>(sb, tl, TM_DKV, j, rows, ntile, crank, L, p.dkv32, gslot(j), abort_flag,
+                                          p.status)))
+        break;
+      if (L == 0) SMLA_STAMP(j, 10);
+      rows = nxt;
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -595,5 +629,16 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
     tc_bwd_h128_kernel<false><<<dim3(2 * nt), dim3(kThreads), kSmemBytes, s>>>(tm_q, tm_do, p);
   return cudaGetLastError();
 }
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_bwd_setup(int tok0) {
+  static const long long z[tc::kTraceCtas * tc::kTracePerCta] = {};
+  if (cudaMemcpyToSymbol(tc::g_trace, z, sizeof(z)) != cudaSuccess) return -1;
+  return cudaMemcpyToSymbol(tc::g_trace_tok0, &tok0, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int smla_trace_bwd_read(long long* dst) {
+  return cudaMemcpyFromSymbol(dst, tc::g_trace, sizeof(long long) * tc::kTraceCtas * tc::kTracePerCta) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 }  // namespace smla

@@ -337,11 +337,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
       : "memory");
 }
 
-// NC consecutive 32-bit columns (NC a multiple of 4, up to 28) from taddr
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v);
+
+// NC consecutive 32-bit columns (NC a multiple of 4, up to 32) from taddr
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
-  static_assert(NC % 4 == 0 && NC <= 28, "columns");
-  if constexpr (NC >= 16) {
+  static_assert(NC % 4 == 0 && NC <= 32, "columns");
+  if constexpr (NC == 32) {
+    tmem_ld32(taddr, v);
+  } else if constexpr (NC >= 16) {
     tmem_ld16(taddr, v);
     if constexpr (NC > 16) tmem_ld_cols<NC - 16>(taddr + 16, v + 16);
   } else if constexpr (NC >= 8) {
