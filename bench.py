@@ -350,6 +350,15 @@ def run_ours(args):
             e2e["ms_per_step"] = max_over_ranks([e2e["ms_per_step"]], dev)[0]
             e2e["value"] = replica_throughput(T, world, e2e["ms_per_step"])
 
+    # the other workloads, measured after the headline's timed region (rank 0 only)
+    others = None
+    if rank == 0 and args.workloads != "none":
+        del out, lse, dq, dkv32, dkv, ws, flush, q, kv, dout, idx, cu
+        torch.cuda.empty_cache()
+        others = {}
+        for c in [int(x) for x in args.workloads.split(",") if x]:
+            others[str(c)] = time_workload(capi, c, dev, args.workload_steps, 2, peaks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = oracle_tokens_per_s(w, args.cpu_seconds)
@@ -365,15 +374,16 @@ def run_ours(args):
                        "sequences": w.B, "l2": "flushed before every timed step (256 MiB write)",
                        "parallelism": "replicas" if world > 1 else "single-gpu"},
             "fwd": {"ms": fwd_ms, "tflops": fwd_flop / (fwd_ms * 1e-3) / 1e12,
-                    "roofline_frac": bound_ms(fwd_flop) / fwd_ms},
+                    "roofline_frac": bound_ms(fwd_flop) / fwd_ms, "gathered_kv_gbs": gbytes / (fwd_ms * 1e-3) / 1e9},
             "bwd": {"ms": bwd_ms, "tflops": bwd_flop / (bwd_ms * 1e-3) / 1e12,
-                    "roofline_frac": bound_ms(bwd_flop) / bwd_ms, "dkv_mode": MODE_NAMES[args.dkv_mode],
-                    "dkv_scatter_bytes": DKV_RED_BYTES_PER_SLOT * n_valid},
+                    "roofline_frac": bound_ms(bwd_flop) / bwd_ms, "gathered_kv_gbs": gbytes / (bwd_ms * 1e-3) / 1e9,
+                    "dkv_mode": MODE_NAMES[args.dkv_mode], "dkv_scatter_bytes": DKV_RED_BYTES_PER_SLOT * n_valid},
             "bwd_other_dkv_mode": other,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
+            "workloads": others,
             "gpu_launches": launches,
             "wall_s_timed": wall,
             "outputs_finite": finite,
@@ -381,6 +391,69 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_workload(capi, cfg: int, dev, steps: int, warmup: int, peaks: dict):
+    """fwd and bwd of workload `cfg` (inputs resident in HBM, L2 flushed before
+    each step): times, TFLOP/s, tokens/s, fractions of the roofline and the
+    achieved rate of gathered KV bytes.  Run after the headline timed region."""
+    import torch
+    w = W.make_workload(cfg)
+    T, H, topk = w.T, w.H, w.topk
+    n_valid = w.n_valid()
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, kv, dout = bf(w.q), bf(w.kv), bf(w.dout)
+    idx = torch.from_numpy(np.ascontiguousarray(w.indices)).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dq = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    dkv32 = torch.empty((T, 1, 576), dtype=torch.float32, device=dev)
+    dkv = torch.empty((T, 1, 576), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(capi.sparse_mla_bwd_workspace_bytes(T, H, topk, 0), 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for k in range(warmup + steps):
+        flush.zero_()
+        if k >= warmup:
+            ev[k - warmup][0].record(stream)
+        capi.sparse_mla_fwd(q, kv, idx, cu, w.scale, out=out, lse=lse)
+        if k >= warmup:
+            ev[k - warmup][1].record(stream)
+        capi.sparse_mla_bwd(q, kv, out, dout, lse, idx, cu, w.scale, dq=dq, dkv_f32=dkv32, dkv=dkv, workspace=ws)
+        if k >= warmup:
+            ev[k - warmup][2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    finite = bool(torch.isfinite(lse).all()) and bool(torch.isfinite(dkv32).all()) and \
+        bool(torch.isfinite(dq.float()).all()) and bool(torch.isfinite(out.float()).all())
+    fwd_flop = FWD_FLOP_PER_SLOT_HEAD * H * n_valid
+    bwd_flop = BWD_FLOP_PER_SLOT_HEAD * H * n_valid
+    gbytes = GATHER_BYTES_PER_SLOT * n_valid
+    tp = peaks["bf16_tflops_sustained"]
+    hbm = peaks["hbm_gbs"]
+
+    def bound_ms(flop):
+        return max(flop / (tp * 1e12), gbytes / (hbm * 1e9)) * 1e3
+
+    def leg(ms, flop):
+        b = bound_ms(flop)
+        return {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
+                "roofline_frac": b / ms, "bound_ms": b,
+                "bound": "tensor" if flop / (tp * 1e12) > gbytes / (hbm * 1e9) else "gathered bytes at HBM",
+                "gathered_kv_gbs": gbytes / (ms * 1e-3) / 1e9}
+
+    res = {"workload": w.name, "T": T, "H": H, "topk": topk, "valid_slots": n_valid, "steps": steps,
+           "fwd": leg(fwd_ms, fwd_flop), "bwd": leg(bwd_ms, bwd_flop),
+           "tokens_per_s": T / ((fwd_ms + bwd_ms) * 1e-3), "outputs_finite": finite}
+    del q, kv, dout, idx, cu, out, lse, dq, dkv32, dkv, ws, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def traffic_record():
@@ -599,6 +672,9 @@ def main():
     ap.add_argument("--config", type=int, default=5, help="workload 1..5 (5 = headline)")
     ap.add_argument("--tokens", type=int, default=0, help="use only the first N tokens (small profiling case)")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--workloads", default="1,2,3,4",
+                    help="other workloads timed after the headline (comma list of 1..4, or 'none')")
+    ap.add_argument("--workload-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -233,10 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(bar_addr(sb, QD_FULL), (5 + 4) * p.H * 128);
+      // q and dO are read once: evict-first, so that they do not push the fp32
+      // dKV lines the reductions keep hitting out of L2
+      const uint64_t pol = l2_evict_first_policy();
       for (int k = 0; k < 5; ++k)
-        tma_load_2d(sb + SM_Q + k * kChunk, &tm_q, 64 * (k < nch ? g0 + k : 8), t * p.H, bar_addr(sb, QD_FULL));
+        tma_load_2d_hint(sb + SM_Q + k * kChunk, &tm_q, 64 * (k < nch ? g0 + k : 8), t * p.H, bar_addr(sb, QD_FULL), pol);
       for (int k = 0; k < 4; ++k)
-        tma_load_2d(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * p.H, bar_addr(sb, QD_FULL));
+        tma_load_2d_hint(sb + SM_DO + k * kChunk, &tm_do, 64 * (g0 + k), t * p.H, bar_addr(sb, QD_FULL), pol);
     }
     // thread pt copies 16-byte piece c16 of rows r0 + 8 j of every chunk
     const int c16 = pt & 7, r0 = pt >> 3;

@@ -1,0 +1,76 @@
+"""Inputs at the edge of the finite domain (slime issue #2201, Summary: the
+fused backward must not turn finite inputs into NaN).
+
+The kernels compute in fp32 on bf16 inputs, so their outputs are finite as long
+as every fp32 dot product and sum they form stays below the fp32 maximum (the
+bound on the inputs is derived beside the kernels' precision readings).  These
+cases push the magnitudes far past the workloads' (q ~ N(0, 8^2), kv ~ N(0, 1)):
+logits of standard deviation 64 (q ~ N(0, 64^2), a near one-hot softmax and LSE
+values in the hundreds), and ten kv rows scaled by 256 (scores and outputs in
+the hundreds to thousands, dq up to ~2.6e5).
+
+Every output must be finite, with no exception.  The relative Frobenius bound
+is the same as everywhere.  The max-abs allowance is an absolute figure for the
+workloads' magnitudes; each rounding step of the path (bf16 P before the PV
+product, fp32 sums of products) errs in proportion to the magnitudes flowing
+through it, so each output is held to the allowance times the factor by which
+that output grows when the inputs grow by c:
+  q scaled by c (c = 8: std 64 against the workloads' 8): scores and LSE grow
+  by c, dkv = dS^T q + P^T dO by c, out and dq (dS K, dS from dO V) by 1;
+  kv rows scaled by c (c = 256): scores, LSE, out (P V) and dkv grow by c, and
+  dq = dS K by c^2, because dS = P (dP - Delta) carries dP = dO V (factor c)
+  and K brings another.
+A CPU simulation of the kernel's rounding (fp32 P, dP and Delta; dS' as bf16
+hi + lo) on the scaled-kv case gives a dq error of about 500 where two
+dominant rows cancel, against terms of 2.6e5: the fp32 arithmetic itself, not
+the kernel, sets that figure."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sparse_mla_ref as orc
+from bwd_sparse_mla_gb300 import capi
+from bwd_sparse_mla_gb300 import workloads as W
+from tests.gpu_helpers import MAX_ABS, assert_close, device_inputs, oracle_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _large_logits():
+    c = 8.0
+    growth = {"out": 1.0, "lse": c, "dq": 1.0, "dkv": c}
+    return W.make_custom(300, 128, 256, [300], seed=91, empty_rows=2, q_std=64.0), growth
+
+
+def _large_kv_rows():
+    w = W.make_custom(300, 16, 256, [300], seed=92, empty_rows=2)
+    kv = orc.bf16_bits_to_f64(w.kv).reshape(w.T, -1)
+    rows = np.random.default_rng(5).choice(w.T, 10, replace=False)
+    kv[rows] *= 256.0                       # exact in bf16 (a power of two)
+    w.kv = W.f32_to_bf16_bits(kv.astype(np.float32)).reshape(w.T, 1, -1)
+    c = 256.0
+    return w, {"out": c, "lse": c, "dq": c * c, "dkv": c}
+
+
+@pytest.mark.parametrize("case", ["large-logits", "large-kv-rows"])
+def test_finite_and_matching_at_large_magnitudes(case, cuda_device):
+    w, growth = _large_logits() if case == "large-logits" else _large_kv_rows()
+    d = device_inputs(w, cuda_device)
+    q, kv, dout = oracle_inputs(w)
+    out, lse = capi.sparse_mla_fwd(d["q"], d["kv"], d["indices"], d["cu_seqlens"], w.scale)
+    dq, dkv32, dkv16 = capi.sparse_mla_bwd(d["q"], d["kv"], out, d["dout"], lse, d["indices"], d["cu_seqlens"],
+                                           w.scale)
+    torch.cuda.synchronize()
+    for name, t in (("out", out), ("lse", lse), ("dq", dq), ("dkv_f32", dkv32), ("dkv", dkv16)):
+        assert int((~torch.isfinite(t.float())).sum()) == 0, f"{case}: non-finite {name}"
+    out_ref, lse_ref = orc.sparse_mla_fwd(q, kv, w.indices, w.scale)
+    dq_ref, dkv_ref = orc.sparse_mla_bwd(q, kv, to_f64(out), dout, to_f64(lse), w.indices, w.scale)
+    failures = []
+    for name, gpu, ref, kind in (("out", to_f64(out), out_ref, "bf16"), ("lse", to_f64(lse), lse_ref, "f32"),
+                                 ("dq", to_f64(dq), dq_ref, "bf16"),
+                                 ("dkv", to_f64(dkv32).reshape(w.T, -1), dkv_ref, "f32")):
+        try:
+            assert_close(name, gpu, ref, kind=kind, abs_tol=MAX_ABS * growth[name])
+        except AssertionError as e:
+            failures.append(f"{case}: {e}")
+    assert not failures, "\n".join(failures)
