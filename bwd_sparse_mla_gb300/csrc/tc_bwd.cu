@@ -27,11 +27,14 @@
 //   MMA      : dQ_half += (hi + lo) K_half (M=128, N=256|320, K=32) and the
 //              transposed dKV tiles dKV^T[d, j] = dO^T (hi + lo) + q^T (hi + lo)
 //              (M=128 dims, N=32 slots, K=128 heads);
-//   drain    : the exchange warps (slot columns 0..19) and the softmax warps
-//              (20..31) read the previous block's dKV tiles from TMEM and add
-//              them into the fp32 dKV rows named by the valid slots (coalesced
-//              128-byte fp32 reductions; padding slots issue no write, the
-//              no-op the miles PR #2079 summary describes for the clamped atomic).
+//   drain    : four drain warps (one per TMEM lane quarter) read each dKV
+//              tile from TMEM as soon as its MMAs complete, hand the tile back
+//              to the MMA issuer at once (one barrier pair per tile, so the next
+//              block's products for that tile overlap the reductions of the
+//              rest), and add it into the fp32 dKV rows named by the valid slots
+//              (coalesced 128-byte fp32 reductions; padding slots issue no
+//              write, the no-op the miles PR #2079 summary describes for the
+//              clamped atomic).
 #include <cuda.h>
 
 #include "smla_common.cuh"
@@ -69,7 +72,7 @@ constexpr int SM_BLIST = SM_BFLAG + kMaxBlocks;         // blocks with a valid s
 constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;        // their number
 constexpr int SM_BAR = SM_NB + 8;
 enum Bar { KV_FULL = 0, KV_EMPTY = 2, QD_FULL = 4, SDP_FULL = 5, SDP_FREE = 6, X_FULL = 7, X_EMPTY = 9,
-           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 14, NBAR = 15 };
+           P_FULL = 11, PDS_FREE = 12, DKV_FULL = 13, DKV_FREE = 16, NBAR = 19 };   // DKV_*: one per tile
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_SMID = SM_TMEM + 8;
 constexpr int SM_ABORT = SM_SMID + 4;
@@ -100,57 +103,78 @@ struct TcBwdParams {
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
 
-// Adds slot columns [C0, C0 + NC) of block j's dKV^T tiles into the fp32 rows
-// the valid slots name.  `rows`: lane k holds the row of slot k (-1 for
-// padding).  Dims of tile m: CTA 0 -> [0,128), [128,256), tail [512,576);
-// CTA 1 -> [256,384), [384,512).  Called by a full set of four warps (one per
-// TMEM lane quarter); each thread arrives once per block on DKV_FREE.  With
-// kStore (deterministic mode) the slot rows are stored at gslot + k * 576
-// (k = slot within the block) instead of added into dkv32.
-template <int C0, int NC, bool kStore>
-__device__ __forceinline__ bool drain_cols(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
-                                           uint32_t crank, int L, float* dkv32, float* gslot, volatile int* abort_flag,
-                                           uint32_t* status) {
-  if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL), j & 1, abort_flag, status))) return false;
-  tc_fence_after();
+// 4 x 4 transpose among the four lanes 4a + b (b = lane & 3): on entry lane
+// 4a + r holds x[c] = M[r][c]; on return y[r] = M[r][b].  Two butterfly
+// exchanges (lane ^ 1, then lane ^ 2), two shuffles each.
+__device__ __forceinline__ void transpose4(float x0, float x1, float x2, float x3, int b, float* y) {
+  // step 1: pairs (b, b ^ 1) swap the columns whose low bit differs from b's
+  const bool o1 = b & 1;
+  const float r0 = __shfl_xor_sync(0xffffffffu, o1 ? x0 : x1, 1);
+  const float r1 = __shfl_xor_sync(0xffffffffu, o1 ? x2 : x3, 1);
+  // t[c2 | j] = M[(b & 2) | j][c2 | (b & 1)]
+  const float t0 = o1 ? r0 : x0, t1 = o1 ? x1 : r0, t2 = o1 ? r1 : x2, t3 = o1 ? x3 : r1;
+  // step 2: pairs (b, b ^ 2) swap the row halves
+  const bool o2 = b & 2;
+  const float v0 = __shfl_xor_sync(0xffffffffu, o2 ? t0 : t2, 2);
+  const float v1 = __shfl_xor_sync(0xffffffffu, o2 ? t1 : t3, 2);
+  y[0] = o2 ? v0 : t0;
+  y[1] = o2 ? v1 : t1;
+  y[2] = o2 ? t2 : v0;
+  y[3] = o2 ? t3 : v1;
+}
+
+// Adds block j's dKV^T tiles into the fp32 rows the valid slots name.  `rows`:
+// lane k holds the row of slot k (-1 for padding).  Dims of tile m: CTA 0 ->
+// [0,128), [128,256), tail [512,576); CTA 1 -> [256,384), [384,512).  Called by
+// the four drain warps (one per TMEM lane quarter).  Tile m is read once its
+// MMAs completed (DKV_FULL + m) and handed back (DKV_FREE + m) before its
+// reductions are issued.  With kStore (deterministic mode) the slot rows are
+// stored at gslot + k * 576 (k = slot within the block) instead of added into
+// dkv32.
+template <bool kStore>
+__device__ __forceinline__ bool drain_tiles(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
+                                            uint32_t crank, int L, float* dkv32, float* gslot,
+                                            volatile int* abort_flag, uint32_t* status) {
 #pragma unroll 1
   for (int m = 0; m < ntile; ++m) {
-    float gh[NC], gl[NC];
-    tmem_ld_cols<NC>(tl + tm_dkv + 64 * m + C0, gh);        // hi half of the slots' columns
-    tmem_ld_cols<NC>(tl + tm_dkv + 64 * m + 32 + C0, gl);   // lo half
-    if (m == ntile - 1) {               // this set's part of every tile is read: the MMA may overwrite them
-      tc_fence_before();
-      mbar_arrive(bar_addr(sb, DKV_FREE));
-    }
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL + m), j & 1, abort_flag, status))) return false;
+    tc_fence_after();
     const int d = (crank == 0 ? (m < 2 ? 128 * m : 512) : 256 + 128 * m) + L;
+    float gh[kBK], gl[kBK];
+    tmem_ld_cols<kBK>(tl + tm_dkv + 64 * m, gh);        // hi half of the slots' columns
+    tmem_ld_cols<kBK>(tl + tm_dkv + 64 * m + 32, gl);   // lo half
+    tc_fence_before();
+    mbar_arrive(bar_addr(sb, DKV_FREE + m));            // the MMA may overwrite this tile
     if (d < kDqk) {                     // warp-uniform: only CTA 0's tail tile has lanes past 576
+      // 4 x 4 transposes among lanes 4a..4a+3: afterwards lane 4a+b holds dims
+      // 4a..4a+3 (of the warp's 32) of slot 4g+b, one 16-byte reduction each
+      const int b = L & 3;              // L & 31 is the lane
+      const int d4 = d - b;             // first of the four dims
 #pragma unroll
-      for (int k = 0; k < NC; ++k) {
-        const int row = __shfl_sync(0xffffffffu, rows, C0 + k);
+      for (int g = 0; g < kBK / 4; ++g) {
+        float y[4];
+        transpose4(gh[4 * g] + gl[4 * g], gh[4 * g + 1] + gl[4 * g + 1], gh[4 * g + 2] + gl[4 * g + 2],
+                   gh[4 * g + 3] + gl[4 * g + 3], b, y);
+        const int k = 4 * g + b;
+        const int row = __shfl_sync(0xffffffffu, rows, k);
         if (row < 0) continue;
         if (kStore)
-          gslot[(C0 + k) * kDqk + d] = gh[k] + gl[k];
+          *reinterpret_cast<float4*>(gslot + k * kDqk + d4) = make_float4(y[0], y[1], y[2], y[3]);
         else
-          red_add_f32(dkv32 + (int64_t)row * kDqk + d, gh[k] + gl[k]);
+          red_add_v4(dkv32 + (int64_t)row * kDqk + d4, y[0], y[1], y[2], y[3]);
       }
     }
   }
   return true;
 }
 
-template <int C0, int NC>
 __device__ __forceinline__ bool drain_any(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
                                           uint32_t crank, int L, float* dkv32, float* gslot, volatile int* abort_flag,
                                           uint32_t* status) {
   return gslot != nullptr
-             ? drain_cols<C0, NC, true>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status)
-             : drain_cols<C0, NC, false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status);
+             ? drain_tiles<true>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status)
+             : drain_tiles<false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status);
 }
-
-// slot columns of each block's dKV tiles drained by the drain warps ([0, kDrainCols))
-// and by the exchange warps (the rest)
-constexpr int kDrainCols = 32;
-constexpr int kXchgDrainCols = kBK - kDrainCols;
 
 // kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
 template <bool kAllHeads>
@@ -178,9 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     *abort_flag = 0;
     mbar_init(bar_addr(sb, KV_FULL + 0), kProducers + 1);   // cp.async arrivals + mask/rows
     mbar_init(bar_addr(sb, KV_FULL + 1), kProducers + 1);
-    // MMA commit + softmax and exchange threads (mask / rows read) + drain threads (rows read)
-    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 256 + 128);
-    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 256 + 128);
+    // MMA commit + softmax threads (mask read) + drain threads (rows read)
+    mbar_init(bar_addr(sb, KV_EMPTY + 0), 1 + 128 + 128);
+    mbar_init(bar_addr(sb, KV_EMPTY + 1), 1 + 128 + 128);
     mbar_init(bar_addr(sb, QD_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FULL), 1);
     mbar_init(bar_addr(sb, SDP_FREE), 256);      // both warp sets loaded the partial S / dP
@@ -190,8 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     mbar_init(bar_addr(sb, X_EMPTY + 1), 128);
     mbar_init(bar_addr(sb, P_FULL), 128);
     mbar_init(bar_addr(sb, PDS_FREE), 1);
-    mbar_init(bar_addr(sb, DKV_FULL), 1);
-    mbar_init(bar_addr(sb, DKV_FREE), kXchgDrainCols > 0 ? 256 : 128);   // the draining warp sets loaded their columns
+    for (int m = 0; m < 3; ++m) {
+      mbar_init(bar_addr(sb, DKV_FULL + m), 1);
+      mbar_init(bar_addr(sb, DKV_FREE + m), 128);   // the drain warps loaded the tile
+    }
     fence_mbar_init();
     *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID) = smid();
   }
@@ -356,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           }
           // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
           //   dKV^T = q_half^T dS' + dO_half^T P   (A MN-major 128B swizzle, B MN-major 64B swizzle)
-          if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE), (j - 1) & 1, abort_flag, p.status))) break;
           SMLA_STAMP(j, 3);
-          tc_fence_after();
-          for (int m = 0; m < ntile; ++m) {
+          for (int m = 0; ok && m < ntile; ++m) {
+            if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE + m), (j - 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
             const uint32_t d_t = tmem + TM_DKV + 64 * m;
             // q^T for this tile: q slots 2m, 2m+1 (CTA 0's tile 2 is the rope tail in slot 4;
             // its second half reads the next buffer and only lands in TMEM lanes that are not drained)
@@ -373,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
                 mma_bf16_ss(d_t, sdesc_add(ddot0, 2 * m * kChunk + ks * 16 * 128), sdesc_add(dpb0, ks * 16 * 128),
                             id_dkv, 1);
             }
+            mma_commit(bar_addr(sb, DKV_FULL + m));
           }
-          mma_commit(bar_addr(sb, DKV_FULL));
+          if (!ok) break;
           mma_commit(bar_addr(sb, PDS_FREE));
           mma_commit(bar_addr(sb, KV_EMPTY + stj));
           SMLA_STAMP(j, 4);
@@ -483,18 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   } else if (warp < kDrainWarp0) {
     // ------------------------------------------------------------ exchange
     // Publishes this CTA's partial S / dP rows of each block to its L2 exchange
-    // slot (the peer's softmax warps read them), then drains its share of the
-    // previous block's dKV tiles (slot columns kDrainCols..31).
+    // slot (the peer's softmax warps read them).
     const int q4 = warp & 3;
     const int L = 32 * q4 + lane;               // TMEM lane: head (exchange) or dim within a tile (drain)
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const int* srows = reinterpret_cast<const int*>(smem + SM_ROWS);
     const uint32_t xfull_peer = mapa(bar_addr(sb, X_FULL), peer);
     const uint32_t my_sm = *reinterpret_cast<volatile uint32_t*>(smem + SM_SMID);
     float4* xmine = reinterpret_cast<float4*>(p.xchg + (size_t)(my_sm % kXchgSlots) * kXchgSlotFloats) + L;
 
     bool ok = true;
-    int prev_rows = -1;
     for (int i = 0; i < nb; ++i) {
       // partial S / dP rows of block i into buffer i & 1 of this SM's slot
       const int xb = i & 1;
@@ -519,28 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       }
       mbar_arrive_remote(xfull_peer + 8 * xb);        // release: our rows are visible to the peer
       if (L == 0) SMLA_STAMP(i, 9);
-      // row list of block i (the mask for the softmax warps is in the same stage)
-      const int st = i & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_FULL + st), (i >> 1) & 1, abort_flag, p.status)))) break;
-      const int rows = srows[st * 32 + lane];
-      mbar_arrive(bar_addr(sb, KV_EMPTY + st));
-      if constexpr (kXchgDrainCols > 0) {
-        if (i >= 1 && !(ok = drain_any<kDrainCols, kXchgDrainCols>(sb, tl, TM_DKV, i - 1, prev_rows, ntile, crank, L,
-                                                                   p.dkv32, gslot(i - 1), abort_flag, p.status)))
-          break;
-      }
-      prev_rows = rows;
-    }
-    if constexpr (kXchgDrainCols > 0) {
-      if (ok && nb > 0)
-        drain_any<kDrainCols, kXchgDrainCols>(sb, tl, TM_DKV, nb - 1, prev_rows, ntile, crank, L, p.dkv32,
-                                              gslot(nb - 1), abort_flag, p.status);
     }
   } else {
     // ------------------------------------------------------------ dKV drain
     // Reads each block's dKV^T tiles from TMEM once the MMAs have written them and
-    // adds them into the fp32 rows the block's valid slots name (slot columns
-    // 0..kDrainCols-1).  A block's row list is read from its KV stage as soon as the
+    // adds them into the fp32 rows the block's valid slots name.  A block's row list is read from its KV stage as soon as the
     // stage lands, one block ahead, so the stage is not held back.
     const int q4 = warp & 3;
     const int L = 32 * q4 + lane;               // TMEM lane: dim within a tile
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     if (nb > 0) ok = read_rows(0, rows);
     for (int j = 0; ok && j < nb; ++j) {
       if (j + 1 < nb && !(ok = read_rows(j + 1, nxt))) break;
-      if (!(ok = drain_any<0, kDrainCols>(sb, tl, TM_DKV, j, rows, ntile, crank, L, p.dkv32, gslot(j), abort_flag,
+      if (!(ok = drain_any(sb, tl, TM_DKV, j, rows, ntile, crank, L, p.dkv32, gslot(j), abort_flag,
                                           p.status)))
         break;
       if (L == 0) SMLA_STAMP(j, 10);

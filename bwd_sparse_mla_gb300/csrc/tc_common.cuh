@@ -84,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ----------------------------------------------------------------- phase trace
-// Built only with -DSMLA_TRACE: clock64 stamps (relative to the CTA's start,
+// Built only with -DSMLA_TRACE: global-timer stamps in ns (relative to the CTA's start,
 // taken after its first cluster barrier) of 33 rows x 12 points for the 8 CTAs
 // starting at 2 * g_trace_tok0; rows outside [0, 33) are not recorded.  The
 // product build compiles the stamps away.
@@ -94,11 +94,11 @@ constexpr int kTracePerCta = 33 * 12;
 // one copy per translation unit (each kernel file reads its own)
 static __device__ long long g_trace[kTraceCtas * kTracePerCta];
 static __device__ int g_trace_tok0;
-#define SMLA_TRACE_T0 const long long trace_t0 = clock64(); const int trace_cta = (int)blockIdx.x - 2 * g_trace_tok0
+#define SMLA_TRACE_T0 const long long trace_t0 = (long long)globaltimer(); const int trace_cta = (int)blockIdx.x - 2 * g_trace_tok0
 #define SMLA_STAMP(i, k)                                                                          \
   do {                                                                                            \
     if (trace_cta >= 0 && trace_cta < kTraceCtas && (i) >= 0 && (i) < 33)                         \
-      g_trace[trace_cta * kTracePerCta + (i) * 12 + (k)] = clock64() - trace_t0;                  \
+      g_trace[trace_cta * kTracePerCta + (i) * 12 + (k)] = (long long)globaltimer() - trace_t0;   \
   } while (0)
 #else
 #define SMLA_TRACE_T0 ((void)0)
