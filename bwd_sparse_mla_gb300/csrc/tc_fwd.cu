@@ -43,9 +43,10 @@ using namespace tc;
 
 constexpr int kBK = 64;                 // slots per block
 constexpr int kProducers = 128;         // warps 0..3 gather
-constexpr int kMmaWarp = 4;             // warp 4: lane 0 issues the MMAs (and the warp owns TMEM), lane 1 moves P
+constexpr int kMmaWarp = 4;             // warp 4: lane 0 issues the MMAs; the warp owns TMEM
 constexpr int kRowWarp0 = 5;            // warps 5..8 (and 9..12 in the score CTA): one thread per head
-constexpr int kThreads = 416;
+constexpr int kAuxWarp = 13;            // warp 13, lane 0: moves P (score CTA) / keeps the P buffers (output CTA)
+constexpr int kThreads = 448;
 constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4 rows, one 16-byte piece of each chunk
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of the 64 rows of a block (8 KiB)
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
@@ -395,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             for (int u = 0; u < kSUnits; ++u, ++n) {
               const int slot = n % kSRing;
               if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
+              SMLA_STAMP(gb - kTraceGb0, u == 0 ? 2 : 5 + u);
               fence_proxy_async_smem();   // cp.async wrote the unit through the generic proxy
               tc_fence_after();
               // S += q K^T over the unit's chunks (A = q from TMEM)
@@ -415,8 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           }
           if (ok) mma_commit(bar_addr(sb, Q_EMPTY));   // q's TMEM may take the next token once these complete
         }
-      } else if (lane == 1) {
-        // P mover: one bulk copy per block from a staging buffer into the output CTA's P buffer
+      }
+      __syncwarp();
+    } else if (warp == kAuxWarp) {
+      if (lane == 0) {
+        // P mover (a warp of its own, so that it never takes issue slots from the
+        // MMA issuer): one bulk copy per block from a staging buffer into the output CTA's P buffer
         const uint32_t pbuf_peer = mapa(sb + SM_P, peer), pfull_peer = mapa(bar_addr(sb, P_FULL), peer);
         int gb = 0;
         bool ok = true;
@@ -632,8 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             SMLA_STAMP(gb - kTraceGb0, 8);
           }
         }
-      } else if (lane == 1) {
-        // P buffer keeper: arms each buffer for its next block's bulk copy and tells the
+      }
+      __syncwarp();
+    } else if (warp == kAuxWarp) {
+      if (lane == 0) {
+        // P buffer keeper (a warp of its own, like the P mover): arms each buffer for its next block's bulk copy and tells the
         // score CTA when PV has finished reading it
         const uint32_t pfree_peer = mapa(bar_addr(sb, P_FREE), peer);
         for (int b = 0; b < kNP; ++b) mbar_arrive_expect_tx(bar_addr(sb, P_FULL + b), kPXBytes);
