@@ -380,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
               if (nch == 5) mma_bf16_ss(tmem + TM_DQ + 256, ad, sdesc_add(dkt0, koff + 4 * kChunkKV), id_dq64, acc);
             }
           }
+          // the KV stage is read only by the S / dP and dQ products: hand it to the
+          // producers before the dKV products, so the gather of block j + 2 starts sooner
+          mma_commit(bar_addr(sb, KV_EMPTY + stj));
           // dKV^T tiles (M = 128 dims, N = 32 slots, K = 128 heads):
           //   dKV^T = q_half^T dS' + dO_half^T P   (A MN-major 128B swizzle, B MN-major 64B swizzle)
           SMLA_STAMP(j, 3);
@@ -403,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           }
           if (!ok) break;
           mma_commit(bar_addr(sb, PDS_FREE));
-          mma_commit(bar_addr(sb, KV_EMPTY + stj));
           SMLA_STAMP(j, 4);
         }
       }
