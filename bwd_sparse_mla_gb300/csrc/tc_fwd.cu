@@ -51,19 +51,22 @@ constexpr int kRowsPerProducer = kBK * 8 / kProducers;   // 4 rows, one 16-byte 
 constexpr int kChunkKV = kBK * 128;     // one 64-dim chunk of the 64 rows of a block (8 KiB)
 constexpr float kLazyRescale = 8.f;     // log2-domain slack before O is rescaled
 constexpr int kMaxBlocks = kTcMaxTopk / kBK;
-constexpr int kNS = 3;                  // score CTA: P staging buffers
+constexpr int kNS = 2;                  // score CTA: P staging buffers
 constexpr int kNP = 3;                  // output CTA: P buffers
 constexpr int kMaskRing = 4;            // score CTA: slot-validity masks of the blocks in flight
 constexpr int kProdBar = 1;             // named barrier of the producer warps
 
-// KV rows are gathered into rings of units: a unit is kUnitCh 64-dim chunks of
-// the 64 rows of a block (128B-swizzled, 8 KiB per chunk, chunks contiguous).
-// A unit is refilled as soon as the MMAs that read it complete, so the gathers
-// stay in flight continuously, across token boundaries.
-//   score CTA:  units of 3 chunks (24 KiB), 3 per block (the 576-wide K rows)
+// KV rows are gathered into rings of units (128B-swizzled, 8 KiB per 64-dim
+// chunk of 64 rows).  A unit is refilled as soon as the MMAs that read it
+// complete, so the gathers stay in flight continuously, across token boundaries.
+//   score CTA:  a token's blocks go in pairs; unit c of a pair holds 64-dim chunk
+//               c of both blocks (16 KiB: the block with an even running index in
+//               the first half), 9 units per pair (the 576-wide K rows), so that
+//               one N = 128 score MMA reads the two blocks as one B operand
 //   output CTA: units of 4 chunks (32 KiB), 2 per block (the 512-wide V rows;
 //               one unit is the B operand of one N = 256 PV MMA)
-constexpr int kSUnitCh = 3, kSUnits = 3, kSRing = 7;
+constexpr int kSPairUnit = 2 * 64 * 128;   // bytes of one score-CTA unit
+constexpr int kSUnitsPerPair = 9, kSRing = 11;
 constexpr int kOUnitCh = 4, kOUnits = 2, kORing = 5;
 
 // one P buffer: 128 heads x 64 slots bf16 (128B swizzle, the PV MMA's A
@@ -73,7 +76,7 @@ constexpr int kPXBytes = kPBytes + 128 * 4;              // what one block hands
 constexpr int kPBufStride = 17 * 1024;                   // 1024-aligned buffer stride
 // score CTA: K ring, P staging, the running state, the mask ring
 constexpr int SM_K = 0;
-constexpr int SM_STG = SM_K + kSRing * kSUnitCh * kChunkKV;
+constexpr int SM_STG = SM_K + kSRing * kSPairUnit;
 constexpr int SM_STATE = SM_STG + kNS * kPBufStride;     // 128 heads x float4 (m, l, l_bf)
 constexpr int SM_MASK = SM_STATE + 128 * 16;             // kMaskRing x u64
 constexpr int kScoreEnd = SM_MASK + 8 * kMaskRing;
@@ -97,7 +100,7 @@ enum ScoreBar { KV_FULL = 0, KV_EMPTY = kSRing, M_FULL = 2 * kSRing, M_EMPTY = M
 enum OutBar { V_FULL = 0, V_EMPTY = kORing, P_FULL = 2 * kORing, R_DONE = P_FULL + kNP, PV_DONE = R_DONE + kNP,
               L_FULL = PV_DONE + kNP, O_FREE = L_FULL + 2, TOK_FULL_O, TOK_EMPTY_O = TOK_FULL_O + 2,
               NBAR_O = TOK_EMPTY_O + 2 };
-constexpr int kNBar = 48;
+constexpr int kNBar = 56;
 static_assert(NBAR_S <= kNBar && NBAR_O <= kNBar, "barrier slots");
 constexpr int SM_TMEM = SM_BAR + 8 * kNBar;
 constexpr int SM_SMID = SM_TMEM + 4;
@@ -107,7 +110,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kSmemBytes > 232448 / 2, "one CTA per SM");
 static_assert(SM_STG % 1024 == 0 && SM_P % 1024 == 0 && kPBufStride % 1024 == 0 && kChunkKV % 1024 == 0, "swizzle atoms");
 static_assert(kPXBytes % 16 == 0 && kPXBytes <= kPBufStride, "bulk copy size");
-static_assert(kSUnitCh * kSUnits == 9 && kOUnitCh * kOUnits == 8, "units cover the rows");
+static_assert(kSPairUnit == 2 * kChunkKV && kOUnitCh * kOUnits == 8, "units cover the rows");
 
 // every accumulator and every tcgen05.ld starts at a column that is a multiple of its width
 constexpr uint32_t kTmemCols = 512;
@@ -143,6 +146,19 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+// 16-byte global load (read-only path) and store with an L2 cache policy
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_v4_hint(uint4* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -287,6 +303,142 @@ __device__ __forceinline__ void produce(const TcFwdParams& p, uint32_t sb, uint8
   }
 }
 
+// Score CTA producers: as produce(), but a token's blocks are gathered in pairs
+// (its listed blocks 2i and 2i + 1): unit c of a pair holds 64-dim chunk c of
+// both blocks, the block with an even running index in the first half, the
+// other in the second.  A token with an odd block count ends with a single
+// block in its half of the unit.  The slot-validity mask of each block goes
+// into the mask ring for the softmax.
+__device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb, uint8_t* smem, int cl, int ncl,
+                                              volatile int* abort_flag SMLA_TRACE_ARGS) {
+  const int pt = threadIdx.x;              // 0..127
+  const int warp = pt >> 5, lane = pt & 31;
+  const int c16 = pt & 7, r0 = pt >> 3;    // 16-byte piece c16 of rows r0 + 16 j of every chunk
+  constexpr int RS = kProducers / 8;
+  constexpr int R = kRowsPerProducer;
+  const int nblk = p.topk / kBK;
+  const int ntok = cluster_tokens(p, cl, ncl);
+  uint8_t* flag = smem + SM_BFLAG;
+  int16_t* blist = reinterpret_cast<int16_t*>(smem + SM_BLIST);
+  volatile int* nbs = reinterpret_cast<volatile int*>(smem + SM_NB);
+  volatile int* tok = reinterpret_cast<volatile int*>(smem + SM_TOK);
+  const uint16_t* kvc = p.kv + 8 * c16;
+  int n = 0, gb = 0;                       // units and blocks gathered so far (all tokens)
+  for (int k = 0; k < ntok; ++k) {
+    const int t = p.t0 + cl + k * ncl;
+    const int32_t* irow = p.indices + (int64_t)t * p.topk;
+    // the blocks of this token that hold a valid slot (0 <= idx < T)
+    for (int b = pt; b < nblk; b += kProducers) {
+      const int4* ib = reinterpret_cast<const int4*>(irow + b * kBK);
+      bool v = false;
+#pragma unroll 4
+      for (int c = 0; c < kBK / 4; ++c) {
+        const int4 x = __ldg(ib + c);
+        v |= (x.x >= 0 && x.x < p.T) | (x.y >= 0 && x.y < p.T) | (x.z >= 0 && x.z < p.T) | (x.w >= 0 && x.w < p.T);
+      }
+      flag[b] = v ? 1 : 0;
+    }
+    named_bar_sync(kProdBar, kProducers);
+    if (warp == 0) {
+      int base = 0;
+      for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const bool f = (b0 + lane < nblk) && flag[b0 + lane];
+        const uint32_t m = __ballot_sync(0xffffffffu, f);
+        if (f) blist[base + __popc(m & ((1u << lane) - 1u))] = (int16_t)(b0 + lane);
+        base += __popc(m);
+      }
+      // publish the token's block count (the slot of token k - 2 must have been read)
+      const bool ok = k < 2 || __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, TOK_EMPTY_S + (k & 1)),
+                                                                 ((k >> 1) - 1) & 1, abort_flag, p.status));
+      if (lane == 0) {
+        *nbs = ok ? base : -1;
+        if (ok) {
+          tok[k & 1] = base;
+          mbar_arrive(bar_addr(sb, TOK_FULL_S + (k & 1)));
+        }
+      }
+    }
+    named_bar_sync(kProdBar, kProducers);
+    const int nb = *nbs;
+    if (nb < 0) return;                    // uniform over the producer warps
+    // rows of this thread and mask lanes of the (up to) two blocks of a pair, one pair ahead
+    int nxt[2][R], nm[2][2];
+    auto fetch = [&](int i) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const bool in = i + q < nb;
+        const int32_t* ib = irow + (in ? blist[i + q] : 0) * kBK;
+#pragma unroll
+        for (int j = 0; j < R; ++j) nxt[q][j] = in ? __ldg(ib + r0 + RS * j) : -1;
+        nm[q][0] = (in && warp == 0) ? __ldg(ib + lane) : -1;
+        nm[q][1] = (in && warp == 0) ? __ldg(ib + 32 + lane) : -1;
+      }
+    };
+    if (nb > 0) fetch(0);
+    bool ok = true;
+    for (int i = 0; ok && i < nb; i += 2) {
+      const int npair = nb - i < 2 ? 1 : 2;
+      int cur[2][R], cm[2][2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) cur[q][j] = nxt[q][j];
+        cm[q][0] = nm[q][0]; cm[q][1] = nm[q][1];
+      }
+      if (i + 2 < nb) fetch(i + 2);
+      const uint16_t* src[2][R];
+      uint32_t dsto[2][R], nbytes[2][R];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int r = r0 + RS * j;
+          const bool v = cur[q][j] >= 0 && cur[q][j] < p.T;
+          src[q][j] = kvc + (int64_t)(v ? cur[q][j] : 0) * kDqk;
+          dsto[q][j] = ((gb + q) & 1) * kChunkKV + r * 128 + ((c16 ^ (r & 7)) << 4);
+          nbytes[q][j] = v ? 16u : 0u;
+        }
+      if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 9);
+#pragma unroll 1
+      for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
+        const int slot = n % kSRing;
+        if (n >= kSRing &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + slot), ((n / kSRing) - 1) & 1, abort_flag,
+                                                     p.status))))
+          break;                           // warp-uniform exit
+        const uint32_t unit = sb + SM_K + slot * kSPairUnit;
+#pragma unroll
+        for (int j = 0; j < R; ++j) cp_async16(unit + dsto[0][j], src[0][j] + 64 * c, nbytes[0][j]);
+        if (npair == 2) {
+#pragma unroll
+          for (int j = 0; j < R; ++j) cp_async16(unit + dsto[1][j], src[1][j] + 64 * c, nbytes[1][j]);
+        }
+        cp_async_arrive(bar_addr(sb, KV_FULL + slot));
+      }
+      if (!ok) break;
+      if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 10);
+      if (warp == 0) {                     // slot validity of the blocks for the softmax
+        for (int q = 0; ok && q < npair; ++q) {
+          const int gbq = gb + q, mr = gbq % kMaskRing;
+          if (gbq >= kMaskRing &&
+              !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, M_EMPTY + mr), ((gbq / kMaskRing) - 1) & 1,
+                                                       abort_flag, p.status))))
+            break;
+          const uint32_t ma = __ballot_sync(0xffffffffu, cm[q][0] >= 0 && cm[q][0] < p.T);
+          const uint32_t mb = __ballot_sync(0xffffffffu, cm[q][1] >= 0 && cm[q][1] < p.T);
+          if (lane == 0) {
+            *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * mr) = (uint64_t)ma | ((uint64_t)mb << 32);
+            mbar_arrive(bar_addr(sb, M_FULL + mr));
+          }
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);    // warp 0's mask waits decide for its warp only
+      gb += npair;
+    }
+    if (!ok) return;
+  }
+}
+
 // Block count of the cluster's token k, from the token ring (one read per
 // calling thread, acknowledged on the ring's empty barrier).  -1 on abort.
 template <bool kWarp>
@@ -375,12 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
   if (crank == 0) {
     // ================================================================ score CTA
     if (warp < kProducers / 32) {
-      produce<kSUnitCh, kSUnits, kSRing, true>(p, sb, smem, cl, ncl, abort_flag, KV_FULL, KV_EMPTY, TOK_FULL_S,
-                                               TOK_EMPTY_S SMLA_TRACE_PASS);
+      produce_score(p, sb, smem, cl, ncl, abort_flag SMLA_TRACE_PASS);
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
-        // MMA issuer: S of each block into buffer gb & 1, unit by unit as the K units land
-        const uint32_t idesc_s = idesc_bf16(128, kBK, false, false);
+        // MMA issuer: S of each pair of blocks, unit by unit as the K units land: one
+        // N = 128 MMA per K step writes both score buffers (buffer b holds the block
+        // with running index parity b); a single last block of a token uses N = 64
+        const uint32_t idesc_s1 = idesc_bf16(128, kBK, false, false);
+        const uint32_t idesc_s2 = idesc_bf16(128, 2 * kBK, false, false);
         const uint64_t dk0 = sdesc_sw128(sb + SM_K, 16, 1024);
         int gb = 0, n = 0;
         bool ok = true;
@@ -388,32 +542,40 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
           if (!(ok = nb >= 0)) break;
           if (!(ok = mbar_wait(bar_addr(sb, Q_FULL), k & 1, abort_flag, p.status))) break;
-          for (int j = 0; ok && j < nb; ++j, ++gb) {
-            const int b = gb & 1;
-            if (gb >= 2 && !(ok = mbar_wait(bar_addr(sb, S_FREE + b), ((gb >> 1) - 1) & 1, abort_flag, p.status))) break;
+          for (int i = 0; ok && i < nb; i += 2) {
+            const int npair = nb - i < 2 ? 1 : 2;
+            for (int q = 0; ok && q < npair; ++q) {   // both score buffers must be free
+              const int gbq = gb + q;
+              if (gbq >= 2) ok = mbar_wait(bar_addr(sb, S_FREE + (gbq & 1)), ((gbq >> 1) - 1) & 1, abort_flag, p.status);
+            }
+            if (!ok) break;
             SMLA_STAMP(gb - kTraceGb0, 0);
+            const int b1 = gb & 1;               // a single block: its buffer and half of the unit
 #pragma unroll 1
-            for (int u = 0; u < kSUnits; ++u, ++n) {
+            for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
               const int slot = n % kSRing;
               if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
-              SMLA_STAMP(gb - kTraceGb0, u == 0 ? 2 : 5 + u);
               fence_proxy_async_smem();   // cp.async wrote the unit through the generic proxy
               tc_fence_after();
-              // S += q K^T over the unit's chunks (A = q from TMEM)
+              // S += q K^T over chunk c (A = q from TMEM)
+              if (npair == 2) {
 #pragma unroll
-              for (int c = 0; c < kSUnitCh; ++c)
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_bf16_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * ks, sdesc_add(dk0, slot * kSPairUnit + ks * 32),
+                              idesc_s2, (c | ks) != 0);
+              } else {
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                  const int kk = u * kSUnitCh + c;
-                  mma_bf16_ts(tmem + TM_S + 64 * b, tmem + TM_Q + 32 * kk + 8 * ks,
-                              sdesc_add(dk0, slot * kSUnitCh * kChunkKV + c * kChunkKV + ks * 32), idesc_s,
-                              (kk | ks) != 0);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_bf16_ts(tmem + TM_S + 64 * b1, tmem + TM_Q + 32 * c + 8 * ks,
+                              sdesc_add(dk0, slot * kSPairUnit + b1 * kChunkKV + ks * 32), idesc_s1, (c | ks) != 0);
+              }
               mma_commit(bar_addr(sb, KV_EMPTY + slot));
             }
             if (!ok) break;
-            mma_commit(bar_addr(sb, S_FULL + b));
+            mma_commit(bar_addr(sb, S_FULL + (gb & 1)));
+            if (npair == 2) mma_commit(bar_addr(sb, S_FULL + ((gb + 1) & 1)));
             SMLA_STAMP(gb - kTraceGb0, 1);
+            gb += npair;
           }
           if (ok) mma_commit(bar_addr(sb, Q_EMPTY));   // q's TMEM may take the next token once these complete
         }
@@ -476,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         tc_fence_after();
         {
           const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk);
+          const uint64_t pol = l2_evict_first_policy();   // q is read once: keep the KV rows in L2
           uint4 v[2][8];
 #pragma unroll
           for (int c0 = 0; c0 < 10; c0 += 4) {     // two chunks of the group per round (loads in flight together)
@@ -484,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
               const int kc = g + c0 + 2 * r;
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                v[r][c] = (real && kc < 9) ? __ldg(qrow + 8 * kc + c) : make_uint4(0u, 0u, 0u, 0u);
+                v[r][c] = (real && kc < 9) ? ld_nc_v4_hint(qrow + 8 * kc + c, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
@@ -715,6 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         tc_fence_after();
         const float inv = 1.f / fmaxf(l_bf, kSumexpFloor);
         uint16_t* orow = p.out + ((int64_t)t * p.H + (real ? h : 0)) * kDv;
+        const uint64_t opol = l2_evict_first_policy();   // out is written once: keep the KV rows in L2
         // every lane of the warp takes part in the warp-collective tcgen05.ld; only
         // the rows of real heads are stored
 #pragma unroll 1
@@ -730,8 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             uint4* dst = reinterpret_cast<uint4*>(orow + 64 * part);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                  pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+              st_v4_hint(dst + c, make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                  pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv)), opol);
           }
         }
         tc_fence_before();
