@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           SMLA_STAMP(j, 3);
           for (int m = 0; ok && m < ntile; ++m) {
             if (j >= 1 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE + m), (j - 1) & 1, abort_flag, p.status))) break;
+            if (m >= 1) SMLA_STAMP(j, m == 1 ? 11 : 8);
             tc_fence_after();
             const uint32_t d_t = tmem + TM_DKV + 64 * m;
             // q^T for this tile: q slots 2m, 2m+1 (CTA 0's tile 2 is the rope tail in slot 4;

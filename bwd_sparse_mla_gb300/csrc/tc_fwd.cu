@@ -555,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
               const int slot = n % kSRing;
               if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
+              if (c == 0 || c == 3 || c == 6 || c == 8) SMLA_STAMP(gb - kTraceGb0, c == 0 ? 2 : c == 3 ? 6 : c == 6 ? 7 : 8);
               fence_proxy_async_smem();   // cp.async wrote the unit through the generic proxy
               tc_fence_after();
               // S += q K^T over chunk c (A = q from TMEM)
