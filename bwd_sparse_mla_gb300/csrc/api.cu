@@ -40,6 +40,9 @@ bool supported_h(int H) { return H == 8 || H == 16 || H == 32 || H == 64 || H ==
 // The tensor-core kernels take every supported H (a 128-row head tile, rows
 // past H zero) up to their top-k limit; larger top-k runs the CUDA-core kernels.
 bool use_tc(int H, int topk) { (void)H; return topk <= smla::kTcMaxTopk; }
+// With at most 16 heads the forward runs the slots-as-rows tensor-core kernel
+// (the heads are the N = 16 columns of its MMAs instead of a 128-row tile).
+bool use_small_fwd(int H) { return H <= 16; }
 
 // The kernels are built for sm_103a only; refuse any other device.
 int check_device() {
@@ -183,7 +186,9 @@ int fwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const int32_t* indices
   a.t0 = t0;
   a.nt = nt;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = use_tc(H, topk) ? smla::launch_fwd_tc(a, s) : smla::launch_fwd_simt(a, s);
+  cudaError_t e = !use_tc(H, topk) ? smla::launch_fwd_simt(a, s)
+                  : use_small_fwd(H) ? smla::launch_fwd_tc_small(a, s)
+                                     : smla::launch_fwd_tc(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_fwd launch");
   count_launches(1);
   return 0;
