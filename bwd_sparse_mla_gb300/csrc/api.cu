@@ -44,6 +44,14 @@ bool use_tc(int H, int topk) { (void)H; return topk <= smla::kTcMaxTopk; }
 // (the heads are the N = 16 columns of its MMAs instead of a 128-row tile).
 bool use_small_fwd(int H) { return H <= 16; }
 
+// The backward kernel for this head count and top-k: the slots-as-rows tensor-core
+// kernel for H <= 16, the 128-row head tile above, the CUDA-core kernels past the
+// tensor-core top-k limit.
+cudaError_t launch_bwd_any(const smla::BwdArgs& a, cudaStream_t s) {
+  if (!use_tc(a.H, a.topk)) return smla::launch_bwd_simt(a, s);
+  return a.H <= 16 ? smla::launch_bwd_tc_small(a, s) : smla::launch_bwd_tc(a, s);
+}
+
 // The kernels are built for sm_103a only; refuse any other device.
 int check_device() {
   int dev = 0;
@@ -251,7 +259,7 @@ int sparse_mla_bwd_rows(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
   a.t0 = t0;
   a.nt = nt;
-  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  e = launch_bwd_any(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd_rows launch");
   count_launches(1);
   return 0;
@@ -316,7 +324,7 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
   if (dkv_mode == SMLA_DKV_ATOMIC) {
-    e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+    e = launch_bwd_any(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
     count_launches(1);
   } else {
@@ -339,7 +347,7 @@ int sparse_mla_bwd(const smla_bf16_t* q, const smla_bf16_t* kv, const smla_bf16_
     for (int t0 = 0; t0 < T; t0 += (int)tc) {
       a.t0 = t0;
       a.nt = (int)((size_t)(T - t0) < tc ? (size_t)(T - t0) : tc);
-      e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+      e = launch_bwd_any(a, s);
       if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd launch");
       e = smla::launch_reduce_rows(offset, seg, pos, gbuf, L.ng, a.gstride, (int64_t)t0 * topk,
                                    (int64_t)(t0 + a.nt) * topk, T, dkv_f32, s);
@@ -424,7 +432,7 @@ int sparse_mla_bwd_noalloc(const smla_bf16_t* q, const smla_bf16_t* kv, const sm
   e = cudaMemsetAsync(dkv_f32, 0, (size_t)T * smla::kDqk * sizeof(float), s);
   if (e != cudaSuccess) return cuda_fail(e, "dkv zeroing");
   smla::BwdArgs a{q, kv, dout, lse, delta, indices, dq, dkv_f32, T, H, topk, scale};
-  e = use_tc(H, topk) ? smla::launch_bwd_tc(a, s) : smla::launch_bwd_simt(a, s);
+  e = launch_bwd_any(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bwd_noalloc launch");
   count_launches(1);
   if (dkv != nullptr) {

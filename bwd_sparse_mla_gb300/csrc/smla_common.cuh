@@ -91,6 +91,7 @@ cudaError_t launch_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaStr
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t launch_fwd_tc_small(const FwdArgs& a, cudaStream_t s);   // H <= 16 (tc_fwd_small.cu)
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s);   // H == 128
+cudaError_t launch_bwd_tc_small(const BwdArgs& a, cudaStream_t s);   // H <= 16 (tc_bwd_small.cu)
 cudaError_t read_tc_status(uint32_t* out, bool clear);
 cudaError_t launch_wait_selftest(cudaStream_t s);
 // deterministic dKV (dkv_det.cu)
