@@ -22,11 +22,13 @@
 //   MMA       : dQ^T[d, h] += K^T dS'^T (M = 128 dims per tile, N = 32 = hi and
 //               lo heads, K = 128 slots) into TMEM across the token's blocks; the
 //               gathered units are then free.  dKV^T[d, j] = q^T (dS'_hi + dS'_lo)
-//               + dO^T (P_hi + P_lo) (M = 128 dims, N = 128 slots, K = 16 heads,
-//               hi and lo as two K steps), one 128-dim tile at a time into two
-//               alternating TMEM buffers;
-//   drain     : four warps (one per TMEM lane quarter: a dim each) load a tile,
-//               hand the buffer back, transpose 4 x 4 lane groups and issue
+//               + dO^T (P_hi + P_lo) (M = 128 dims, N = 64 slots, K = 16 heads,
+//               hi and lo as two K steps), ten tiles per block (five 128-dim
+//               ranges x two halves of the slots) through four TMEM buffers;
+//   drain     : the drain warps (even tiles) and the slot warps (odd tiles, after
+//               handing over P / dS'), four warps per set, one per TMEM lane
+//               quarter (a dim each): load a whole tile, hand the buffer back at
+//               once, transpose 4 x 4 lane groups and issue
 //               16-byte fp32 reductions into the rows the valid slots name
 //               (padding slots issue no write).  Deterministic mode: the rows
 //               are stored per slot instead.
@@ -73,7 +75,7 @@ constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;
 constexpr int SM_BAR = (SM_NB + 8 + 7) & ~7;
 enum Bar { LAT_FULL = 0, LAT_EMPTY = kNLat, TAIL_FULL = 2 * kNLat, TAIL_EMPTY = TAIL_FULL + kNTail,
            QD_FULL = TAIL_EMPTY + kNTail, QD_EMPTY, RL_FULL, RL_EMPTY = RL_FULL + kRing, SD_FULL = RL_EMPTY + kRing,
-           SD_FREE, P_FULL, PDS_FREE, DQ_DONE, DQ_FREE, DKV_FULL, DKV_FREE = DKV_FULL + 2, TOK_FULL = DKV_FREE + 2,
+           SD_FREE, P_FULL, PDS_FREE, DQ_DONE, DQ_FREE, DKV_FULL, DKV_FREE = DKV_FULL + 4, TOK_FULL = DKV_FREE + 4,
            TOK_EMPTY = TOK_FULL + 2, NBAR = TOK_EMPTY + 2 };
 constexpr int SM_TMEM = SM_BAR + 8 * NBAR;
 constexpr int SM_ABORT = SM_TMEM + 4;
@@ -84,7 +86,7 @@ static_assert(SM_TAIL % 1024 == 0 && SM_Q % 1024 == 0 && SM_DO % 1024 == 0 && SM
               "swizzle atoms");
 
 // TMEM: S^T and dP^T (16 columns each), dQ^T as five 32-column tiles (hi | lo
-// heads; the fifth holds the rope dims in lanes 0..63), two 128-column dKV^T buffers
+// heads; the fifth holds the rope dims in lanes 0..63), four 64-column dKV^T buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_S = 0, TM_DP = 16, TM_DQ = 64, TM_DKV = 256;
 
@@ -137,6 +139,48 @@ __device__ __forceinline__ void transpose4(float x0, float x1, float x2, float x
   y[1] = o2 ? v1 : t1;
   y[2] = o2 ? t2 : v0;
   y[3] = o2 ? t3 : v1;
+}
+
+// Drains dKV^T tile tt of block gb (dims 128 (tt / 2).., slots 64 (tt % 2)..) by
+// one set of four warps (one per TMEM lane quarter: dim L of the tile): loads
+// the tile's 64 slot columns, hands the TMEM buffer back, then adds each valid
+// slot's value into its kv row (4 x 4 lane transposes, 16-byte reductions), or
+// stores it per slot in the deterministic mode.  rows[c]: lane k holds the row
+// of slot 32 c + k of the block (-1 for padding).
+__device__ __forceinline__ bool drain_tile(const SmallBwdParams& p, uint32_t sb, uint32_t tl, int L, int lane,
+                                           int gb, int tt, const int (&rows)[4], float* gblk,
+                                           volatile int* abort_flag) {
+  const int n = 10 * gb + tt;               // tiles issued so far
+  const int bb = n & 3, m = tt >> 1, hh = tt & 1, b4 = lane & 3;
+  if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL + bb), (n >> 2) & 1, abort_flag, p.status)))
+    return false;
+  tc_fence_after();
+  float g[64];                               // the tile's 64 slots of this dim
+  tmem_ld64(tl + TM_DKV + 64 * bb, g);
+  tc_fence_before();
+  mbar_arrive(bar_addr(sb, DKV_FREE + bb));  // the MMA may overwrite this buffer
+  const int d = 128 * m + L;                 // dims 512..575 in the last range: lanes 0..63
+  if (d < kDqk) {                            // warp-uniform
+    const int d4 = d - b4;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int gq = 0; gq < 8; ++gq) {
+        float y[4];
+        transpose4(g[32 * c + 4 * gq], g[32 * c + 4 * gq + 1], g[32 * c + 4 * gq + 2], g[32 * c + 4 * gq + 3], b4, y);
+        const int kk = 4 * gq + b4;
+        const int rsrc = c == 0 ? (hh ? rows[2] : rows[0]) : (hh ? rows[3] : rows[1]);
+        const int row = __shfl_sync(0xffffffffu, rsrc, kk);
+        if (row < 0) continue;
+        if (gblk != nullptr)
+          *reinterpret_cast<float4*>(gblk + (int64_t)(64 * hh + 32 * c + kk) * kDqk + d4) =
+              make_float4(y[0], y[1], y[2], y[3]);
+        else
+          red_add_v4(p.dkv32 + (int64_t)row * kDqk + d4, y[0], y[1], y[2], y[3]);
+      }
+    }
+  }
+  return true;
 }
 
 // Producers: per token, list the blocks of 128 slots that hold a valid slot,
@@ -318,9 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
     mbar_init(bar_addr(sb, PDS_FREE), 1);
     mbar_init(bar_addr(sb, DQ_DONE), 1);
     mbar_init(bar_addr(sb, DQ_FREE), 128);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       mbar_init(bar_addr(sb, DKV_FULL + b), 1);
       mbar_init(bar_addr(sb, DKV_FREE + b), 128);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(bar_addr(sb, TOK_FULL + b), 1);
       mbar_init(bar_addr(sb, TOK_EMPTY + b), 1 + 128 + 128);   // MMA thread, slot threads, drain threads
     }
@@ -341,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
     if (lane == 0) {
       const uint32_t id_sd = idesc_bf16(128, kHN, false, false);        // A = K / V rows, B = q / dO rows (K-major)
       const uint32_t id_dq = idesc_bf16(128, 2 * kHN, true, false);     // A = K^T (MN-major), B = dS'^T (K-major)
-      const uint32_t id_dkv = idesc_bf16(128, kBS, true, false);        // A = q^T / dO^T (MN-major), B = slot rows
+      const uint32_t id_dkv = idesc_bf16(128, kBS / 2, true, false);    // A = q^T / dO^T (MN-major), B = 64 slot rows
       const uint64_t dlat = sdesc_sw128(sb + SM_LAT, 16, 1024);
       const uint64_t dlatt = sdesc_sw128(sb + SM_LAT, 128 * 128, 1024);
       const uint64_t dtail = sdesc_sw128(sb + SM_TAIL, 16, 1024);
@@ -411,19 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
                         sdesc_add(ddst, (ks >> 2) * 32 * 128 + (ks & 3) * 32), id_dq, (i > 0 || ks > 0));
           mma_commit(bar_addr(sb, TAIL_EMPTY + ts));
           if (i + 1 == nb) mma_commit(bar_addr(sb, DQ_DONE));
-          // dKV^T tiles: q^T (dS'_hi + dS'_lo) [+ dO^T (P_hi + P_lo) inside the value range]
+          // dKV^T tiles (dims 128 m.., slots 64 hh..): q^T (dS'_hi + dS'_lo)
+          // [+ dO^T (P_hi + P_lo) inside the value range]
 #pragma unroll 1
-          for (int m = 0; m < 5; ++m, ++nt2) {
-            const int bb = nt2 & 1;
-            if (nt2 >= 2 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE + bb), ((nt2 >> 1) - 1) & 1, abort_flag, p.status)))
+          for (int tt = 0; tt < 10; ++tt, ++nt2) {
+            const int m = tt >> 1, hh = tt & 1;
+            const int bb = nt2 & 3;
+            if (nt2 >= 4 && !(ok = mbar_wait(bar_addr(sb, DKV_FREE + bb), ((nt2 >> 2) - 1) & 1, abort_flag, p.status)))
               break;
             tc_fence_after();
-            const uint32_t d_t = tmem + TM_DKV + 128 * bb;
-            mma_bf16_ss(d_t, sdesc_add(dqt, 2 * m * kQChunk), drows, id_dkv, 0);
-            mma_bf16_ss(d_t, sdesc_add(dqt, 2 * m * kQChunk), sdesc_add(drows, 32), id_dkv, 1);
+            const uint32_t d_t = tmem + TM_DKV + 64 * bb;
+            const uint64_t rb = sdesc_add(drows, hh * 64 * 128);
+            mma_bf16_ss(d_t, sdesc_add(dqt, 2 * m * kQChunk), rb, id_dkv, 0);
+            mma_bf16_ss(d_t, sdesc_add(dqt, 2 * m * kQChunk), sdesc_add(rb, 32), id_dkv, 1);
             if (m < 4) {
-              mma_bf16_ss(d_t, sdesc_add(ddot, 2 * m * kQChunk), sdesc_add(drows, 64), id_dkv, 1);
-              mma_bf16_ss(d_t, sdesc_add(ddot, 2 * m * kQChunk), sdesc_add(drows, 96), id_dkv, 1);
+              mma_bf16_ss(d_t, sdesc_add(ddot, 2 * m * kQChunk), sdesc_add(rb, 64), id_dkv, 1);
+              mma_bf16_ss(d_t, sdesc_add(ddot, 2 * m * kQChunk), sdesc_add(rb, 96), id_dkv, 1);
             }
             mma_commit(bar_addr(sb, DKV_FULL + bb));
           }
@@ -470,6 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
                                                      p.status))))
           break;
         const bool valid = reinterpret_cast<volatile const int*>(rlist)[rr * kBS + L] >= 0;
+        int rows[4];                       // for the odd dKV tiles this warp set drains
+#pragma unroll
+        for (int c = 0; c < 4; ++c) rows[c] = reinterpret_cast<volatile const int*>(rlist)[rr * kBS + 32 * c + lane];
+        const int sbase = reinterpret_cast<volatile const int*>(smem + SM_RBASE)[rr];
         mbar_arrive(bar_addr(sb, RL_EMPTY + rr));
         uint32_t dh[kHN / 2], dlo[kHN / 2], ph[kHN / 2], plo[kHN / 2];
 #pragma unroll
@@ -512,6 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
         fence_proxy_async_smem();          // the MMAs read them through the async proxy
         tc_fence_before();
         mbar_arrive(bar_addr(sb, P_FULL));
+        // this warp set drains the block's odd dKV tiles (the drain warps the even ones)
+        float* gblk = p.gbuf == nullptr ? nullptr : p.gbuf + ((int64_t)(t - p.t0) * p.topk + sbase) * kDqk;
+#pragma unroll 1
+        for (int tt = 1; ok && tt < 10; tt += 2) ok = drain_tile(p, sb, tl, L, lane, gb, tt, rows, gblk, abort_flag);
       }
       if (!ok) break;
       // epilogue: dq[t, h, d] = dQ^T hi + lo columns; lane L holds dim L of each 128-dim tile
@@ -548,8 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
     const int L = 32 * q4 + lane;          // TMEM lane: dim within a tile
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int* rlist = reinterpret_cast<const int*>(smem + SM_RLIST);
-    const int b4 = lane & 3;
-    int gb = 0, nt2 = 0;
+    int gb = 0;
     bool ok = true;
     for (int k = 0; ok && k < ntok; ++k) {
       const int t = p.t0 + (int)blockIdx.x + k * (int)gridDim.x;
@@ -568,40 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_small_kernel(SmallBwdParam
         // deterministic mode: where the contributions of this block's slots go
         float* gblk = p.gbuf == nullptr ? nullptr : p.gbuf + ((int64_t)(t - p.t0) * p.topk + sbase) * kDqk;
 #pragma unroll 1
-        for (int m = 0; m < 5; ++m, ++nt2) {
-          const int bb = nt2 & 1;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL + bb), (nt2 >> 1) & 1, abort_flag,
-                                                       p.status))))
-            break;
-          tc_fence_after();
-          const int d = 128 * m + L;        // dims 512..575 in the fifth tile: lanes 0..63
-          const bool live = d < kDqk;       // warp-uniform
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {     // 32 slots at a time
-            float g[32];
-            tmem_ld32(tl + TM_DKV + 128 * bb + 32 * c, g);
-            if (c == 3) {
-              tc_fence_before();
-              mbar_arrive(bar_addr(sb, DKV_FREE + bb));   // the MMA may overwrite this buffer
-            }
-            if (live) {
-              const int d4 = d - b4;
-#pragma unroll
-              for (int gq = 0; gq < 8; ++gq) {
-                float y[4];
-                transpose4(g[4 * gq], g[4 * gq + 1], g[4 * gq + 2], g[4 * gq + 3], b4, y);
-                const int kk = 4 * gq + b4;
-                const int row = __shfl_sync(0xffffffffu, rows[c], kk);
-                if (row < 0) continue;
-                if (gblk != nullptr) {
-                  *reinterpret_cast<float4*>(gblk + (int64_t)(32 * c + kk) * kDqk + d4) = make_float4(y[0], y[1], y[2], y[3]);
-                } else {
-                  red_add_v4(p.dkv32 + (int64_t)row * kDqk + d4, y[0], y[1], y[2], y[3]);
-                }
-              }
-            }
-          }
-        }
+        for (int tt = 0; ok && tt < 10; tt += 2) ok = drain_tile(p, sb, tl, L, lane, gb, tt, rows, gblk, abort_flag);
       }
     }
   }
