@@ -192,13 +192,42 @@ __global__ void __launch_bounds__(256) reduce_rows_kernel(const int* __restrict_
   float* row = dkv32 + (int64_t)r * kDqk + lane;
 #pragma unroll
   for (int k = 0; k < kDqk / 32; ++k) acc[k] = row[32 * k];
-  for (; p < e; ++p) {
-    const int64_t s = seg[p];
-    if (s >= slot_hi) break;
-    const float* gs = gbuf + (s - slot_lo) * kDqk + lane;
-    for (int g = 0; g < ng; ++g) {
+  if (ng == 1) {
+    // four contributions in flight at a time, added in ascending slot order (the
+    // row's slot list is sorted, so the ones in this chunk form a prefix)
+    for (;;) {
+      int64_t s[4];
 #pragma unroll
-      for (int k = 0; k < kDqk / 32; ++k) acc[k] += gs[(int64_t)g * gstride + 32 * k];
+      for (int u = 0; u < 4; ++u) s[u] = p + u < e ? (int64_t)seg[p + u] : slot_hi;
+      float v[4][kDqk / 32];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (s[u] < slot_hi) {
+          const float* gs = gbuf + (s[u] - slot_lo) * kDqk + lane;
+#pragma unroll
+          for (int k = 0; k < kDqk / 32; ++k) v[u][k] = gs[32 * k];
+        }
+      }
+      int n = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (s[u] >= slot_hi) break;
+#pragma unroll
+        for (int k = 0; k < kDqk / 32; ++k) acc[k] += v[u][k];
+        ++n;
+      }
+      p += n;
+      if (n < 4) break;
+    }
+  } else {
+    for (; p < e; ++p) {
+      const int64_t s = seg[p];
+      if (s >= slot_hi) break;
+      const float* gs = gbuf + (s - slot_lo) * kDqk + lane;
+      for (int g = 0; g < ng; ++g) {
+#pragma unroll
+        for (int k = 0; k < kDqk / 32; ++k) acc[k] += gs[(int64_t)g * gstride + 32 * k];
+      }
     }
   }
 #pragma unroll
