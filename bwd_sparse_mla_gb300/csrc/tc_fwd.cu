@@ -7,7 +7,9 @@
 //
 //   score CTA (cluster rank 0) holds the current token's q (128 heads x 576
 //     dims, bf16) in TMEM as the A operand and gathers the full 576-wide KV
-//     rows named by each block of 64 top-k slots.  Per block it computes the
+//     rows named by each block of 64 top-k slots.  q itself arrives through
+//     the same ring of units as the KV rows (nine 64-dim chunks ahead of the
+//     token's first block) and is copied into TMEM by the tensor pipe.  Per block it computes the
 //     complete scores S = q K^T (M = 128 heads, N = 64 slots, K = 576).  Two
 //     softmax groups (one thread per head each) take alternate blocks: padding
 //     slots are masked to -inf, the running max moves lazily (only when a
@@ -62,7 +64,9 @@ constexpr int kProdBar = 1;             // named barrier of the producer warps
 //   score CTA:  a token's blocks go in pairs; unit c of a pair holds 64-dim chunk
 //               c of both blocks (16 KiB: the block with an even running index in
 //               the first half), 9 units per pair (the 576-wide K rows), so that
-//               one N = 128 score MMA reads the two blocks as one B operand
+//               one N = 128 score MMA reads the two blocks as one B operand; a
+//               token with a valid block starts with 9 q units (unit c: 64-dim
+//               chunk c of the token's 128 head rows, rows past H zero)
 //   output CTA: units of 4 chunks (32 KiB), 2 per block (the 512-wide V rows;
 //               one unit is the B operand of one N = 256 PV MMA)
 constexpr int kSPairUnit = 2 * 64 * 128;   // bytes of one score-CTA unit
@@ -94,7 +98,7 @@ constexpr int SM_NB = SM_BLIST + 2 * kMaxBlocks;
 constexpr int SM_BAR = (SM_NB + 8 + 7) & ~7;
 // barriers: the same slots carry role-specific meanings
 enum ScoreBar { KV_FULL = 0, KV_EMPTY = kSRing, M_FULL = 2 * kSRing, M_EMPTY = M_FULL + kMaskRing,
-                Q_FULL = M_EMPTY + kMaskRing, Q_EMPTY, S_FULL, S_FREE = S_FULL + 2, ST_FULL = S_FREE + 2,
+                Q_EMPTY = M_EMPTY + kMaskRing, S_FULL, S_FREE = S_FULL + 2, ST_FULL = S_FREE + 2,
                 STG_FULL = ST_FULL + 2, STG_FREE = STG_FULL + kNS, P_FREE = STG_FREE + kNS, L_EMPTY = P_FREE + kNP,
                 TOK_FULL_S = L_EMPTY + 2, TOK_EMPTY_S = TOK_FULL_S + 2, NBAR_S = TOK_EMPTY_S + 2 };
 enum OutBar { V_FULL = 0, V_EMPTY = kORing, P_FULL = 2 * kORing, R_DONE = P_FULL + kNP, PV_DONE = R_DONE + kNP,
@@ -153,6 +157,18 @@ __device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p), "l"(pol));
   return v;
+}
+// 16-byte cp.async (zero fill past src_bytes) with an L2 cache policy
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src), "r"(src_bytes),
+               "l"(pol)
+               : "memory");
+}
+// Tensor-pipe copy of a 128-row x 32-byte shared-memory matrix (described like an
+// MMA operand) into 128 TMEM lanes x 8 columns; executes after the tcgen05 copies
+// and before the MMAs that the same thread issues later
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void st_v4_hint(uint4* p, uint4 v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -376,6 +392,36 @@ __device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb,
     };
     if (nb > 0) fetch(0);
     bool ok = true;
+    if (nb > 0) {                          // the token's q rows, chunk by chunk, ahead of its blocks
+      const uint64_t pol = l2_evict_first_policy();   // q is read once: keep the KV rows in L2
+      const uint16_t* qsrc[2][R];
+      uint32_t qdst[2][R], qbytes[2][R];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int r = r0 + RS * j, h = 64 * q + r;
+          const bool v = h < p.H;
+          qsrc[q][j] = p.q + ((int64_t)t * p.H + (v ? h : 0)) * kDqk + 8 * c16;
+          qdst[q][j] = q * kChunkKV + r * 128 + ((c16 ^ (r & 7)) << 4);
+          qbytes[q][j] = v ? 16u : 0u;
+        }
+#pragma unroll 1
+      for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
+        const int slot = n % kSRing;
+        if (n >= kSRing &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + slot), ((n / kSRing) - 1) & 1, abort_flag,
+                                                     p.status))))
+          break;                           // warp-uniform exit
+        const uint32_t unit = sb + SM_K + slot * kSPairUnit;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int j = 0; j < R; ++j) cp_async16_hint(unit + qdst[q][j], qsrc[q][j] + 64 * c, qbytes[q][j], pol);
+        cp_async_arrive(bar_addr(sb, KV_FULL + slot));
+      }
+      if (!ok) return;
+    }
     for (int i = 0; ok && i < nb; i += 2) {
       const int npair = nb - i < 2 ? 1 : 2;
       int cur[2][R], cm[2][2];
@@ -478,7 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         mbar_init(bar_addr(sb, M_FULL + k), 1);
         mbar_init(bar_addr(sb, M_EMPTY + k), 128);             // the softmax group read the mask
       }
-      mbar_init(bar_addr(sb, Q_FULL), 256);                    // both groups stored their chunks of q
       mbar_init(bar_addr(sb, Q_EMPTY), 1);                     // the token's score MMAs completed
       for (int g = 0; g < 2; ++g) {
         mbar_init(bar_addr(sb, S_FULL + g), 1);
@@ -536,12 +581,29 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         const uint32_t idesc_s1 = idesc_bf16(128, kBK, false, false);
         const uint32_t idesc_s2 = idesc_bf16(128, 2 * kBK, false, false);
         const uint64_t dk0 = sdesc_sw128(sb + SM_K, 16, 1024);
-        int gb = 0, n = 0;
+        int gb = 0, n = 0, kq = 0;           // kq: tokens with a valid block so far
         bool ok = true;
         for (int k = 0; ok && k < ntok; ++k) {
           const int nb = read_token<false>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
           if (!(ok = nb >= 0)) break;
-          if (!(ok = mbar_wait(bar_addr(sb, Q_FULL), k & 1, abort_flag, p.status))) break;
+          if (nb == 0) continue;             // no q units, no MMAs
+          // the token's q units into TMEM, once the previous token's score MMAs (which
+          // read q's columns) completed; the MMAs issued after the copies see them
+#pragma unroll 1
+          for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
+            const int slot = n % kSRing;
+            if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
+            if (c == 0 && kq >= 1 && !(ok = mbar_wait(bar_addr(sb, Q_EMPTY), (kq - 1) & 1, abort_flag, p.status)))
+              break;
+            fence_proxy_async_smem();
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tmem_cp_128x256b(tmem + TM_Q + 32 * c + 8 * ks, sdesc_add(dk0, slot * kSPairUnit + ks * 32));
+            mma_commit(bar_addr(sb, KV_EMPTY + slot));
+          }
+          if (!ok) break;
+          ++kq;
           for (int i = 0; ok && i < nb; i += 2) {
             const int npair = nb - i < 2 ? 1 : 2;
             for (int q = 0; ok && q < npair; ++q) {   // both score buffers must be free
@@ -578,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             SMLA_STAMP(gb - kTraceGb0, 1);
             gb += npair;
           }
-          if (ok) mma_commit(bar_addr(sb, Q_EMPTY));   // q's TMEM may take the next token once these complete
+          if (ok) mma_commit(bar_addr(sb, Q_EMPTY));   // q's columns may take the next token once these complete
         }
       }
       __syncwarp();
@@ -632,34 +694,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         const int t = p.t0 + cl + k * ncl;
         const int nb = read_token<true>(p, sb, smem, k, TOK_FULL_S, TOK_EMPTY_S, abort_flag);
         if (!(ok = nb >= 0)) break;
-        // this token's q into TMEM (the A operand of the score MMAs) once the previous
-        // token's score MMAs completed: group g stores chunks g, g + 2, ...
-        if (k >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, Q_EMPTY), (k - 1) & 1, abort_flag, p.status))))
-          break;
-        tc_fence_after();
-        {
-          const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk);
-          const uint64_t pol = l2_evict_first_policy();   // q is read once: keep the KV rows in L2
-          uint4 v[2][8];
-#pragma unroll
-          for (int c0 = 0; c0 < 10; c0 += 4) {     // two chunks of the group per round (loads in flight together)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int kc = g + c0 + 2 * r;
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                v[r][c] = (real && kc < 9) ? ld_nc_v4_hint(qrow + 8 * kc + c, pol) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int kc = g + c0 + 2 * r;
-              if (kc < 9) tmem_st32(tl + TM_Q + 32 * kc, reinterpret_cast<const float*>(v[r]));
-            }
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar_addr(sb, Q_FULL));
         if (real && k + 1 < ntok) {            // the next token's q row into L2
           const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q + ((int64_t)(t + ncl) * p.H + h) * kDqk);
           for (int c = g; c < 9; c += 2) prefetch_l2(qn + 128 * c);
