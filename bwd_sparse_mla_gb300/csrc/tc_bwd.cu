@@ -421,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     const bool real = h < p.H;
     const float lse2 = real ? p.lse[(int64_t)t * p.H + h] * kLog2e : INFINITY;
     const float dl = real ? p.delta[(int64_t)t * p.H + h] : 0.f;
+    const uint64_t c2x2 = f32x2(p.c2, p.c2), nlse2x2 = f32x2(-lse2, -lse2);
+    const uint64_t scale2 = f32x2(p.scale, p.scale), dl2x2 = f32x2(dl, dl);
     uint8_t* prow = smem + SM_P + h * 128;
     uint8_t* dsrow = smem + SM_DS + h * 128;
     const int sw = h & 7;               // 128B swizzle: 16-byte chunk index ^= row & 7
@@ -461,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       // P / dS' buffers are free once this CTA's dQ / dKV MMAs of the previous block completed
       if (i >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PDS_FREE), (i - 1) & 1, abort_flag, p.status))))
         break;
-      // P and dS' as bf16 pairs hi + lo, 8 slots (one 16-byte chunk of each half-row) at a time
+      // P and dS' as bf16 pairs hi + lo, 8 slots (one 16-byte chunk of each half-row) at a
+      // time; two slots per paired fp32 instruction:
+      //   P = exp2(S c2 - lse2), dS' = (scale P)(dP - Delta), lo = value - hi
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pp[4], dd[4], dl2[4], pl[4];
@@ -469,13 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 4 * c + jj;
           const bool v0 = (mask >> (2 * j)) & 1u, v1 = (mask >> (2 * j + 1)) & 1u;
-          const float p0 = v0 ? ex2(s[2 * j] * p.c2 - lse2) : 0.f;   // padding: P = 0 exactly
-          const float p1 = v1 ? ex2(s[2 * j + 1] * p.c2 - lse2) : 0.f;
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(s[2 * j], s[2 * j + 1]), c2x2, nlse2x2), a0, a1);
+          const float p0 = v0 ? ex2(a0) : 0.f;   // padding: P = 0 exactly
+          const float p1 = v1 ? ex2(a1) : 0.f;
+          const uint64_t pv = f32x2(p0, p1);
           pp[jj] = pack_bf16x2(p0, p1);
-          pl[jj] = pack_bf16x2(p0 - bf16_lo(pp[jj]), p1 - bf16_hi(pp[jj]));
-          const float d0 = p.scale * p0 * (dp[2 * j] - dl), d1 = p.scale * p1 * (dp[2 * j + 1] - dl);
+          float r0, r1;
+          f32x2_split(sub_f32x2(pv, f32x2(bf16_lo(pp[jj]), bf16_hi(pp[jj]))), r0, r1);
+          pl[jj] = pack_bf16x2(r0, r1);
+          const uint64_t dv = mul_f32x2(mul_f32x2(scale2, pv), sub_f32x2(f32x2(dp[2 * j], dp[2 * j + 1]), dl2x2));
+          float d0, d1;
+          f32x2_split(dv, d0, d1);
           dd[jj] = pack_bf16x2(d0, d1);
-          dl2[jj] = pack_bf16x2(d0 - bf16_lo(dd[jj]), d1 - bf16_hi(dd[jj]));   // the part bf16 dropped
+          f32x2_split(sub_f32x2(dv, f32x2(bf16_lo(dd[jj]), bf16_hi(dd[jj]))), r0, r1);   // the part bf16 dropped
+          dl2[jj] = pack_bf16x2(r0, r1);
         }
         *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
         *reinterpret_cast<uint4*>(prow + (((c + 4) ^ sw) << 4)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
