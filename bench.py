@@ -487,6 +487,21 @@ def kernel_source_hash() -> str:
 E2E_CHUNKS = 16
 
 
+def e2e_ranges(T: int, chunks: int = E2E_CHUNKS):
+    """Row ranges of the streamed step: E2E_CHUNKS equal ranges, except that the
+    first and the last are split into ranges of 1/8, 1/4 and 1/2 of a chunk (growing
+    at the start, shrinking at the end), so that less of the first upload and of the
+    last download is left outside the overlap."""
+    c = T / chunks
+    sizes = [c / 8, c / 8, c / 4, c / 2] + [c] * (chunks - 2) + [c / 2, c / 4, c / 8, c / 8]
+    bounds, acc = [0], 0.0
+    for x in sizes:
+        acc += x
+        bounds.append(min(T, round(acc)))
+    bounds[-1] = T
+    return [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(len(sizes)) if bounds[i + 1] > bounds[i]]
+
+
 def same_results(host, device, dev, rows=4096):
     """The streamed step's host results against the device-resident step's (same
     inputs): out, lse and dq bit for bit; dkv, the bf16 of an fp32 sum taken in
@@ -509,11 +524,12 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     """Same step through the public API from pinned host buffers: H2D of the
     inputs, forward, backward, D2H of out, lse, dq and dkv (bf16), all inside the
     timed region.  The step streams through the device in E2E_CHUNKS ranges of
-    query rows (sparse_mla_fwd_rows / sparse_mla_bwd_rows / sparse_mla_dkv_cast):
-    the forward of a range starts as soon as its q and indices have landed, dO
-    uploads while the forward runs, each range's out / lse and dq download while
-    later ranges compute, and dkv (fp32, accumulated over all ranges) is cast
-    and downloaded last.  Copies run on their own streams."""
+    query rows (sparse_mla_fwd_rows / sparse_mla_bwd_rows / sparse_mla_dkv_cast),
+    each range's forward followed by its backward: a range starts as soon as its
+    q and indices have landed, its dO uploads while its forward runs, its out /
+    lse and dq download while later ranges compute, and dkv (fp32, accumulated
+    over all ranges) is cast and downloaded last.  Copies run on their own
+    streams, so uploads and downloads keep pace with the ranges' compute."""
     import torch
     T, H, topk = w.T, w.H, w.topk
     pin = lambda t: t.pin_memory()  # noqa: E731
@@ -538,8 +554,7 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     # ranges alternate between two compute streams: they are independent (their dKV
     # contributions add commutatively), so one range's tail overlaps the next one's work
     comp = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
-    bounds = [round(i * T / E2E_CHUNKS) for i in range(E2E_CHUNKS + 1)]
-    ranges = [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(E2E_CHUNKS) if bounds[i + 1] > bounds[i]]
+    ranges = e2e_ranges(T)
 
     def one(start):
         ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -550,24 +565,21 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
             d_kv.copy_(hkv, non_blocking=True)
             d_cu.copy_(hcu, non_blocking=True)
             ev_meta.record(s_in)
-            for c, (t0, nt) in enumerate(ranges):
+            for c, (t0, nt) in enumerate(ranges):      # range by range: q, indices, then dO
                 d_q[t0:t0 + nt].copy_(hq[t0:t0 + nt], non_blocking=True)
                 d_idx[t0:t0 + nt].copy_(hidx[t0:t0 + nt], non_blocking=True)
                 ev_q[c].record(s_in)
-            for c, (t0, nt) in enumerate(ranges):       # overlaps the forward
                 d_do[t0:t0 + nt].copy_(hdo[t0:t0 + nt], non_blocking=True)
                 ev_do[c].record(s_in)
         cs.wait_event(start)
         d_dkv32.zero_()                                # the row-range backward adds into it
         ev_zero.record(cs)
-        for c, (t0, nt) in enumerate(ranges):
+        for c, (t0, nt) in enumerate(ranges):          # each range's forward, then its backward
             st = comp[c % 2]
             st.wait_event(ev_meta)
             st.wait_event(ev_q[c])
             capi.sparse_mla_fwd_rows(d_q, d_kv, d_idx, d_cu, w.scale, t0, nt, d_out, d_lse, stream=st)
             ev_f[c].record(st)
-        for c, (t0, nt) in enumerate(ranges):
-            st = comp[c % 2]
             st.wait_event(ev_do[c])
             st.wait_event(ev_zero)
             capi.sparse_mla_bwd_rows(d_q, d_kv, d_out, d_do, d_lse, d_idx, d_cu, w.scale, t0, nt, d_dq, d_dkv32, ws,
@@ -582,7 +594,6 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
                 s_out.wait_event(ev_f[c])
                 o_out[t0:t0 + nt].copy_(d_out[t0:t0 + nt], non_blocking=True)
                 o_lse[t0:t0 + nt].copy_(d_lse[t0:t0 + nt], non_blocking=True)
-            for c, (t0, nt) in enumerate(ranges):
                 s_out.wait_event(ev_b[c])
                 o_dq[t0:t0 + nt].copy_(d_dq[t0:t0 + nt], non_blocking=True)
             s_out.wait_event(ev_cast)
@@ -608,9 +619,9 @@ def run_e2e(args, capi, w, dev, h_q, h_kv, h_dout, h_idx, h_cu):
     # for bit, dkv (bf16 of an fp32 sum in another order) within one bf16 step
     return {"value": T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps, "chunks": len(ranges), "dkv_mode": "atomic",
-            "overlap": f"streamed in {len(ranges)} ranges of query rows on two alternating compute streams: q / "
-                       "indices upload overlaps the forward of earlier ranges, dO upload the forward, out / lse and "
-                       "dq download later ranges' work (separate copy streams)",
+            "overlap": f"streamed in {len(ranges)} ranges of query rows (tapered at both ends) on two alternating "
+                       "compute streams, each range's forward then backward: a range's q / indices / dO upload and "
+                       "its out / lse / dq download overlap other ranges' work (separate copy streams)",
             "_host": (o_out, o_lse, o_dq, o_dkv)}
 
 

@@ -80,3 +80,14 @@ def test_streamed_results_are_compared_exactly_except_dkv():
     dkv3 = dkv.clone()
     dkv3[5, 0, 2] = dkv3[5, 0, 2] * 2 + 1                               # far off
     assert not bench.same_results((out, lse, dq, dkv3), (out, lse, dq, dkv), dev, rows=16)
+
+
+@pytest.mark.parametrize("T", [1, 5, 17, 4096, 65536, 65537])
+def test_streamed_ranges_partition_the_rows(T):
+    r = bench.e2e_ranges(T)
+    assert r[0][0] == 0 and sum(n for _, n in r) == T
+    assert all(n > 0 for _, n in r)
+    assert all(r[i][0] + r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+    if T >= 16 * bench.E2E_CHUNKS:          # the edges taper: first and last ranges are the smallest
+        sizes = [n for _, n in r]
+        assert sizes[0] < max(sizes) and sizes[-1] < max(sizes)
