@@ -41,18 +41,27 @@ def _run(cmd: list) -> None:
         sys.stderr.write(r.stderr)
 
 
-def build(extra_flags: list | None = None) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(extra_flags: list | None = None, lib: str = LIB, obj: str = OBJ) -> str:
+    """Compile every translation unit and link `lib` (objects under `obj`).  The
+    debug build (extra_flags=["-DSMLA_DEBUG"]) goes to its own paths, e.g.
+    debug_paths(), so that it never replaces the product library."""
+    os.makedirs(obj, exist_ok=True)
     cc = nvcc()
     flags = CFLAGS + list(extra_flags or [])
     srcs = sources()
-    objs = [os.path.join(OBJ, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(obj, os.path.basename(s)[:-3] + ".o") for s in srcs]
     with ThreadPoolExecutor(max_workers=max(1, len(srcs))) as ex:
         list(ex.map(lambda so: _run([cc, *ARCH, *flags, "-c", so[0], "-o", so[1]]), zip(srcs, objs)))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([cc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def debug_paths() -> tuple:
+    """(library, object folder) of the bounds-checked debug build."""
+    d = os.path.join(PKG, "_build_debug")
+    return os.path.join(d, "libsparse_mla_debug.so"), d
 
 
 if __name__ == "__main__":

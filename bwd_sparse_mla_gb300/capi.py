@@ -63,6 +63,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_launch_count.restype = ctypes.c_uint64
     lib.sparse_mla_wait_selftest.argtypes = [P]
     lib.sparse_mla_wait_selftest.restype = I
+    lib.sparse_mla_bounds_selftest.argtypes = [P]
+    lib.sparse_mla_bounds_selftest.restype = I
     lib.sparse_mla_topk.argtypes = [P, ctypes.c_int64, I, I, P, I, I, P, P]
     lib.sparse_mla_topk.restype = I
     _lib = lib
@@ -92,6 +94,13 @@ def sparse_mla_wait_selftest(stream=None) -> None:
     up after 1 s and sets the device status word to 1 (read and clear it with
     sparse_mla_device_status(clear=True))."""
     _check(load().sparse_mla_wait_selftest(_stream(stream)))
+
+
+def sparse_mla_bounds_selftest(stream=None) -> None:
+    """Debug build only (-DSMLA_DEBUG): enqueue the bounds-check self-test; both of
+    its probes fall outside their buffer, so the device status word becomes 2.  The
+    product build refuses it (-ENOSYS)."""
+    _check(load().sparse_mla_bounds_selftest(_stream(stream)))
 
 
 def sparse_mla_topk(scores, cu_seqlens, topk: int, ncols: int | None = None, indices=None, stream=None):

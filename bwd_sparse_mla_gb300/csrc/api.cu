@@ -146,6 +146,20 @@ int sparse_mla_wait_selftest(void* stream) {
   return 0;
 }
 
+int sparse_mla_bounds_selftest(void* stream) {
+  g_last_error.clear();
+#ifdef SMLA_DEBUG
+  if (int r = check_device()) return r;
+  cudaError_t e = smla::launch_bounds_selftest(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_bounds_selftest launch");
+  count_launches(1);
+  return 0;
+#else
+  (void)stream;
+  return fail(-ENOSYS, "device bounds checks are compiled only into the debug build (-DSMLA_DEBUG)");
+#endif
+}
+
 int sparse_mla_topk(const float* scores, int64_t ld, int T, int ncols, const int32_t* cu_seqlens, int B, int topk,
                     int32_t* indices, void* stream) {
   g_last_error.clear();

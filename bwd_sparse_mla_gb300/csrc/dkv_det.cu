@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(256) copy_ints_kernel(const int* __restrict__ 
 __global__ void __launch_bounds__(256) reduce_rows_kernel(const int* __restrict__ offset, const int* __restrict__ seg,
                                                           int* __restrict__ pos, const float* __restrict__ gbuf,
                                                           int ng, int64_t gstride, int64_t slot_lo, int64_t slot_hi,
-                                                          int T, float* __restrict__ dkv32) {
+                                                          int T, float* __restrict__ dkv32, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int r = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if (r >= T) return;
@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(256) reduce_rows_kernel(const int* __restrict_
   const int e = offset[r + 1];
   if (p >= e || seg[p] >= slot_hi) return;
   float acc[kDqk / 32];
+  if (!check_range(dkv32 + (int64_t)r * kDqk, kDqk, dkv32, (int64_t)T * kDqk, status)) return;
   float* row = dkv32 + (int64_t)r * kDqk + lane;
+  const int64_t gbuf_n = (int64_t)ng * gstride;
 #pragma unroll
   for (int k = 0; k < kDqk / 32; ++k) acc[k] = row[32 * k];
   if (ng == 1) {
@@ -204,8 +206,9 @@ __global__ void __launch_bounds__(256) reduce_rows_kernel(const int* __restrict_
       for (int u = 0; u < 4; ++u) {
         if (s[u] < slot_hi) {
           const float* gs = gbuf + (s[u] - slot_lo) * kDqk + lane;
+          const bool in = check_range(gs - lane, kDqk, gbuf, gbuf_n, status);
 #pragma unroll
-          for (int k = 0; k < kDqk / 32; ++k) v[u][k] = gs[32 * k];
+          for (int k = 0; k < kDqk / 32; ++k) v[u][k] = in ? gs[32 * k] : 0.f;
         }
       }
       int n = 0;
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(256) reduce_rows_kernel(const int* __restrict_
       if (s >= slot_hi) break;
       const float* gs = gbuf + (s - slot_lo) * kDqk + lane;
       for (int g = 0; g < ng; ++g) {
+        if (!check_range(gs - lane + (int64_t)g * gstride, kDqk, gbuf, gbuf_n, status)) continue;
 #pragma unroll
         for (int k = 0; k < kDqk / 32; ++k) acc[k] += gs[(int64_t)g * gstride + 32 * k];
       }
@@ -269,7 +273,8 @@ cudaError_t launch_reduce_rows(const int* offset, const int* seg, int* pos, cons
                                int64_t gstride, int64_t slot_lo, int64_t slot_hi, int T, float* dkv32,
                                cudaStream_t s) {
   reduce_rows_kernel<<<(unsigned)(((int64_t)T * 32 + 255) / 256), 256, 0, s>>>(offset, seg, pos, gbuf, ng, gstride,
-                                                                                slot_lo, slot_hi, T, dkv32);
+                                                                                slot_lo, slot_hi, T, dkv32,
+                                                                                tc_status_ptr());
   return cudaGetLastError();
 }
 

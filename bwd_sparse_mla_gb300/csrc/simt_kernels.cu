@@ -46,7 +46,7 @@ __device__ __forceinline__ void stage_rows_f32(float* dst, int pitch, const uint
 // fp32 (zero rows for padding).  Returns false (uniformly) when no slot of
 // the block is valid.
 __device__ __forceinline__ bool gather_block(const int32_t* idx_row, int blk, int T,
-                                             const uint16_t* kv, int* s_row, float* skv) {
+                                             const uint16_t* kv, int* s_row, float* skv, uint32_t* status) {
   int valid = 0;
   if (threadIdx.x < kBK) {
     const int idx = __ldg(idx_row + blk * kBK + threadIdx.x);
@@ -58,7 +58,8 @@ __device__ __forceinline__ bool gather_block(const int32_t* idx_row, int blk, in
     const int j = i / (kDqk / 8), c = i - j * (kDqk / 8);
     const int row = s_row[j];
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (row >= 0) v = __ldg(reinterpret_cast<const uint4*>(kv + (int64_t)row * kDqk + c * 8));
+    const uint16_t* src = kv + (int64_t)(row >= 0 ? row : 0) * kDqk + c * 8;
+    if (row >= 0 && check_range(src, 8, kv, (int64_t)T * kDqk, status)) v = __ldg(reinterpret_cast<const uint4*>(src));
     float4* d = reinterpret_cast<float4*>(skv + j * kQP + c * 8);
     d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
     d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kNT, 1) fwd_simt_kernel(FwdArgs a) {
   const int32_t* idx_row = a.indices + (int64_t)t * a.topk;
   const int nblk = a.topk / kBK;
   for (int blk = 0; blk < nblk; ++blk) {
-    if (!gather_block(idx_row, blk, a.T, a.kv, s_row, skv)) continue;
+    if (!gather_block(idx_row, blk, a.T, a.kv, s_row, skv, a.status)) continue;
     // scores: lane = slot, heads warp + 8k
     float s[KH];
 #pragma unroll
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_simt_kernel(BwdArgs a) {
   const int32_t* idx_row = a.indices + (int64_t)t * a.topk;
   const int nblk = a.topk / kBK;
   for (int blk = 0; blk < nblk; ++blk) {
-    if (!gather_block(idx_row, blk, a.T, a.kv, s_row, skv)) continue;
+    if (!gather_block(idx_row, blk, a.T, a.kv, s_row, skv, a.status)) continue;
     // S = q.k over 576 dims and dP = dO.v over 512 dims; lane = slot
     float s[KH], dp[KH];
 #pragma unroll
@@ -280,11 +281,15 @@ __global__ void __launch_bounds__(kNT, 1) bwd_simt_kernel(BwdArgs a) {
         float* dst = a.gbuf + (int64_t)blockIdx.y * a.gstride +
                      ((int64_t)(t - a.t0) * a.topk + (int64_t)blk * kBK + kj) * kDqk + kd0;
 #pragma unroll
-        for (int n = 0; n < NK; ++n) *reinterpret_cast<float4*>(dst + 32 * n) = g[n];
+        for (int n = 0; n < NK; ++n)
+          if (check_range(dst + 32 * n, 4, a.gbuf, a.gbuf_floats, a.status))
+            *reinterpret_cast<float4*>(dst + 32 * n) = g[n];
       } else {
         float* dst = a.dkv32 + (int64_t)row * kDqk + kd0;
 #pragma unroll
-        for (int n = 0; n < NK; ++n) red_add_v4(dst + 32 * n, g[n].x, g[n].y, g[n].z, g[n].w);
+        for (int n = 0; n < NK; ++n)
+          if (check_range(dst + 32 * n, 4, a.dkv32, (int64_t)a.T * kDqk, a.status))
+            red_add_v4(dst + 32 * n, g[n].x, g[n].y, g[n].z, g[n].w);
       }
     }
     __syncthreads();
@@ -392,7 +397,9 @@ cudaError_t bwd_launch(const BwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
+cudaError_t launch_fwd_simt(const FwdArgs& args, cudaStream_t s) {
+  FwdArgs a = args;
+  a.status = tc_status_ptr();
   if (a.H == 8) return fwd_launch<8>(a, s);
   if (a.H == 16) return fwd_launch<16>(a, s);
   return fwd_launch<32>(a, s);  // H = 32, 64, 128 in groups of 32 heads
@@ -400,7 +407,10 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
 
 int simt_head_groups(int H) { return H <= 16 ? 1 : H / 32; }
 
-cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
+cudaError_t launch_bwd_simt(const BwdArgs& args, cudaStream_t s) {
+  BwdArgs a = args;
+  a.status = tc_status_ptr();
+  a.gbuf_floats = a.gbuf != nullptr ? (int64_t)simt_head_groups(a.H) * a.gstride : 0;
   if (a.H == 8) return bwd_launch<8>(a, s);
   if (a.H == 16) return bwd_launch<16>(a, s);
   return bwd_launch<32>(a, s);

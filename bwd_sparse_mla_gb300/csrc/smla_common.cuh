@@ -29,6 +29,7 @@ struct FwdArgs {
   float scale;
   // query rows [t0, t0 + nt) of this launch (nt < 0: all T rows)
   int t0 = 0, nt = -1;
+  uint32_t* status = nullptr;   // device status word (debug-build bounds checks)
 };
 
 struct BwdArgs {
@@ -49,6 +50,8 @@ struct BwdArgs {
   // instead of adding it into dkv32
   float* gbuf = nullptr;
   int64_t gstride = 0;
+  int64_t gbuf_floats = 0;      // extent of gbuf (debug-build bounds checks)
+  uint32_t* status = nullptr;   // device status word (debug-build bounds checks)
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -88,6 +91,44 @@ __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// ----------------------------------------------------------------- debug bounds checks
+// Device status word code of a failed bounds check (the word also carries the
+// bounded waits' timeout code 1; see sparse_mla_device_status).
+constexpr uint32_t kErrBounds = 2u;
+// The device status word (lives in tc_fwd.cu).
+uint32_t* tc_status_ptr();
+
+// Debug build (-DSMLA_DEBUG): every gathered 16-byte source and every scatter
+// destination (and the row reads of the deterministic reduction) is checked against
+// its buffer [lo, lo + n) before the access.  A failed check records kErrBounds in
+// the status word (first error wins) and the access is skipped: a gather copies zero
+// bytes from the buffer's start, a scatter or read is not issued.  Nothing traps.
+// In other builds the checks compile to nothing.
+template <typename T>
+__device__ __forceinline__ void check_src(const T*& src, uint32_t& bytes, const T* lo, int64_t n, uint32_t* status) {
+#ifdef SMLA_DEBUG
+  if (src < lo || src + 16 / sizeof(T) > lo + n) {
+    if (status != nullptr) atomicCAS(status, 0u, kErrBounds);
+    src = lo;
+    bytes = 0u;
+  }
+#else
+  (void)src; (void)bytes; (void)lo; (void)n; (void)status;
+#endif
+}
+template <typename T>
+__device__ __forceinline__ bool check_range(const T* ptr, int count, const T* lo, int64_t n, uint32_t* status) {
+#ifdef SMLA_DEBUG
+  if (ptr < lo || ptr + count > lo + n) {
+    if (status != nullptr) atomicCAS(status, 0u, kErrBounds);
+    return false;
+  }
+#else
+  (void)ptr; (void)count; (void)lo; (void)n; (void)status;
+#endif
+  return true;
+}
+
 // 16-byte vector fp32 reduction into global memory (sm_90+).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
@@ -118,6 +159,7 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s);   // H == 128
 cudaError_t launch_bwd_tc_small(const BwdArgs& a, cudaStream_t s);   // H <= 16 (tc_bwd_small.cu)
 cudaError_t read_tc_status(uint32_t* out, bool clear);
 cudaError_t launch_wait_selftest(cudaStream_t s);
+cudaError_t launch_bounds_selftest(cudaStream_t s);
 // deterministic dKV (dkv_det.cu)
 int64_t det_scan_tiles(int T);
 cudaError_t launch_build_row_lists(const int32_t* indices, int T, int topk, int* offset, int* cursor, int* pos,

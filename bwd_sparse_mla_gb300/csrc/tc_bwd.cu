@@ -134,7 +134,8 @@ __device__ __forceinline__ void transpose4(float x0, float x1, float x2, float x
 template <bool kStore>
 __device__ __forceinline__ bool drain_tiles(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
                                             uint32_t crank, int L, float* dkv32, float* gslot,
-                                            volatile int* abort_flag, uint32_t* status) {
+                                            volatile int* abort_flag, uint32_t* status, int64_t dkv_n,
+                                            const float* gbuf, int64_t gbuf_n) {
 #pragma unroll 1
   for (int m = 0; m < ntile; ++m) {
     if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(sb, DKV_FULL + m), j & 1, abort_flag, status))) return false;
@@ -158,10 +159,13 @@ __device__ __forceinline__ bool drain_tiles(uint32_t sb, uint32_t tl, uint32_t t
         const int k = 4 * g + b;
         const int row = __shfl_sync(0xffffffffu, rows, k);
         if (row < 0) continue;
-        if (kStore)
-          *reinterpret_cast<float4*>(gslot + k * kDqk + d4) = make_float4(y[0], y[1], y[2], y[3]);
-        else
-          red_add_v4(dkv32 + (int64_t)row * kDqk + d4, y[0], y[1], y[2], y[3]);
+        if (kStore) {
+          float* dst = gslot + k * kDqk + d4;
+          if (check_range(dst, 4, gbuf, gbuf_n, status)) *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+        } else {
+          float* dst = dkv32 + (int64_t)row * kDqk + d4;
+          if (check_range(dst, 4, dkv32, dkv_n, status)) red_add_v4(dst, y[0], y[1], y[2], y[3]);
+        }
       }
     }
   }
@@ -170,10 +174,12 @@ __device__ __forceinline__ bool drain_tiles(uint32_t sb, uint32_t tl, uint32_t t
 
 __device__ __forceinline__ bool drain_any(uint32_t sb, uint32_t tl, uint32_t tm_dkv, int j, int rows, int ntile,
                                           uint32_t crank, int L, float* dkv32, float* gslot, volatile int* abort_flag,
-                                          uint32_t* status) {
+                                          uint32_t* status, int64_t dkv_n, const float* gbuf, int64_t gbuf_n) {
   return gslot != nullptr
-             ? drain_tiles<true>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status)
-             : drain_tiles<false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status);
+             ? drain_tiles<true>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status, dkv_n,
+                                 gbuf, gbuf_n)
+             : drain_tiles<false>(sb, tl, tm_dkv, j, rows, ntile, crank, L, dkv32, gslot, abort_flag, status, dkv_n,
+                                  gbuf, gbuf_n);
 }
 
 // kAllHeads: H == 128, no padding rows (the exchange then has no per-row test)
@@ -302,7 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         const bool v = cur[j] >= 0 && cur[j] < p.T;
         const uint16_t* src = kvc + (int64_t)(v ? cur[j] : 0) * kDqk;
         const uint32_t dst = stage + r * 128 + ((c16 ^ (r & 7)) << 4);
-        for (int k = 0; k < nch; ++k) cp_async16(dst + k * kChunkKV, src + 64 * k, v ? 16u : 0u);
+        for (int k = 0; k < nch; ++k) {
+          const uint16_t* s = src + 64 * k;
+          uint32_t bytes = v ? 16u : 0u;
+          check_src(s, bytes, p.kv, (int64_t)p.T * kDqk, p.status);
+          cp_async16(dst + k * kChunkKV, s, bytes);
+        }
       }
       cp_async_arrive(bar_addr(sb, KV_FULL + st));
       if (warp == 0) {                        // slot mask and row list of the block
@@ -580,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     if (nb > 0) ok = read_rows(0, rows);
     for (int j = 0; ok && j < nb; ++j) {
       if (j + 1 < nb && !(ok = read_rows(j + 1, nxt))) break;
-      if (!(ok = drain_any(sb, tl, TM_DKV, j, rows, ntile, crank, L, p.dkv32, gslot(j), abort_flag,
-                                          p.status)))
+      if (!(ok = drain_any(sb, tl, TM_DKV, j, rows, ntile, crank, L, p.dkv32, gslot(j), abort_flag, p.status,
+                           (int64_t)p.T * kDqk, p.gbuf, (int64_t)(gridDim.x >> 1) * p.topk * kDqk)))
         break;
       if (L == 0) SMLA_STAMP(j, 10);
       rows = nxt;

@@ -172,11 +172,14 @@ __device__ __forceinline__ bool drain_tile(const SmallBwdParams& p, uint32_t sb,
         const int rsrc = c == 0 ? (hh ? rows[2] : rows[0]) : (hh ? rows[3] : rows[1]);
         const int row = __shfl_sync(0xffffffffu, rsrc, kk);
         if (row < 0) continue;
-        if (gblk != nullptr)
-          *reinterpret_cast<float4*>(gblk + (int64_t)(64 * hh + 32 * c + kk) * kDqk + d4) =
-              make_float4(y[0], y[1], y[2], y[3]);
-        else
-          red_add_v4(p.dkv32 + (int64_t)row * kDqk + d4, y[0], y[1], y[2], y[3]);
+        if (gblk != nullptr) {
+          float* dst = gblk + (int64_t)(64 * hh + 32 * c + kk) * kDqk + d4;
+          if (check_range(dst, 4, p.gbuf, (int64_t)p.nt * p.topk * kDqk, p.status))
+            *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+        } else {
+          float* dst = p.dkv32 + (int64_t)row * kDqk + d4;
+          if (check_range(dst, 4, p.dkv32, (int64_t)p.T * kDqk, p.status)) red_add_v4(dst, y[0], y[1], y[2], y[3]);
+        }
       }
     }
   }
@@ -248,9 +251,12 @@ __device__ __forceinline__ void produce(const SmallBwdParams& p, uint32_t sb, ui
       const uint16_t* dsrc = p.dout + ((int64_t)t * p.H + (real ? h : 0)) * kDv + 8 * c16;
       const uint32_t o = h * 128 + ((c16 ^ (h & 7)) << 4);
 #pragma unroll
-      for (int c = 0; c < 9; ++c) cp_async16(sb + SM_Q + c * kQChunk + o, qsrc + 64 * c, real ? 16u : 0u);
+      for (int c = 0; c < 9; ++c)
+        gather16(sb + SM_Q + c * kQChunk + o, qsrc + 64 * c, real ? 16u : 0u, p.q, (int64_t)p.T * p.H * kDqk, p.status);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) cp_async16(sb + SM_DO + c * kQChunk + o, dsrc + 64 * c, real ? 16u : 0u);
+      for (int c = 0; c < 8; ++c)
+        gather16(sb + SM_DO + c * kQChunk + o, dsrc + 64 * c, real ? 16u : 0u, p.dout, (int64_t)p.T * p.H * kDv,
+                 p.status);
       cp_async_arrive(bar_addr(sb, QD_FULL));
     }
     int nxt[R], nrl[4];
@@ -312,8 +318,8 @@ __device__ __forceinline__ void produce(const SmallBwdParams& p, uint32_t sb, ui
         const uint32_t unit = sb + SM_LAT + slot * kLatBytes;
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-          cp_async16(unit + dsto[j], src[j] + 128 * u, nbytes[j]);
-          cp_async16(unit + 128 * 128 + dsto[j], src[j] + 128 * u + 64, nbytes[j]);
+          gather16(unit + dsto[j], src[j] + 128 * u, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
+          gather16(unit + 128 * 128 + dsto[j], src[j] + 128 * u + 64, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
         }
         cp_async_arrive(bar_addr(sb, LAT_FULL + slot));
       }
@@ -325,7 +331,7 @@ __device__ __forceinline__ void produce(const SmallBwdParams& p, uint32_t sb, ui
         break;
       const uint32_t tunit = sb + SM_TAIL + ts * kTailBytes;
 #pragma unroll
-      for (int j = 0; j < R; ++j) cp_async16(tunit + dsto[j], src[j] + 512, nbytes[j]);
+      for (int j = 0; j < R; ++j) gather16(tunit + dsto[j], src[j] + 512, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
       cp_async_arrive(bar_addr(sb, TAIL_FULL + ts));
     }
     if (!ok) return;

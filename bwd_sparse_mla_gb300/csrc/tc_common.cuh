@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "smla_common.cuh"
+
 namespace smla {
 namespace tc {
 
@@ -217,6 +219,12 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
 // and reads nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// cp_async16 of 16 bytes of the bf16 buffer [lo, lo + n), its source checked in the debug build
+__device__ __forceinline__ void gather16(uint32_t dst, const uint16_t* src, uint32_t src_bytes, const uint16_t* lo,
+                                         int64_t n, uint32_t* status) {
+  check_src(src, src_bytes, lo, n, status);
+  cp_async16(dst, src, src_bytes);
 }
 // Arrive on `bar` once all cp.async previously issued by this thread have
 // completed (the barrier's expected count must include this arrival).

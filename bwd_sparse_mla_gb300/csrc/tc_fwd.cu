@@ -289,7 +289,12 @@ __device__ __forceinline__ void produce(const TcFwdParams& p, uint32_t sb, uint8
 #pragma unroll
         for (int j = 0; j < kRowsPerProducer; ++j)
 #pragma unroll
-          for (int c = 0; c < UCH; ++c) cp_async16(unit + dsto[j] + c * kChunkKV, src[j] + 64 * (u * UCH + c), nbytes[j]);
+          for (int c = 0; c < UCH; ++c) {
+            const uint16_t* s = src[j] + 64 * (u * UCH + c);
+            uint32_t bytes = nbytes[j];
+            check_src(s, bytes, p.kv, (int64_t)p.T * kDqk, p.status);
+            cp_async16(unit + dsto[j] + c * kChunkKV, s, bytes);
+          }
         cp_async_arrive(bar_addr(sb, full0 + slot));
       }
       if (!ok) break;
@@ -410,7 +415,12 @@ __device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb,
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int j = 0; j < R; ++j) cp_async16_hint(unit + qdst[q][j], qsrc[q][j] + 64 * c, qbytes[q][j], pol);
+          for (int j = 0; j < R; ++j) {
+            const uint16_t* s = qsrc[q][j] + 64 * c;
+            uint32_t bytes = qbytes[q][j];
+            check_src(s, bytes, p.q, (int64_t)p.T * p.H * kDqk, p.status);
+            cp_async16_hint(unit + qdst[q][j], s, bytes, pol);
+          }
         cp_async_arrive(bar_addr(sb, KV_FULL + slot));
       }
       if (!ok) return;
@@ -447,10 +457,15 @@ __device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb,
           break;                           // warp-uniform exit
         const uint32_t unit = sb + SM_K + slot * kSPairUnit;
 #pragma unroll
-        for (int j = 0; j < R; ++j) cp_async16(unit + dsto[0][j], src[0][j] + 64 * c, nbytes[0][j]);
-        if (npair == 2) {
+        for (int q = 0; q < 2; ++q) {
+          if (q == 1 && npair < 2) break;
 #pragma unroll
-          for (int j = 0; j < R; ++j) cp_async16(unit + dsto[1][j], src[1][j] + 64 * c, nbytes[1][j]);
+          for (int j = 0; j < R; ++j) {
+            const uint16_t* s = src[q][j] + 64 * c;
+            uint32_t bytes = nbytes[q][j];
+            check_src(s, bytes, p.kv, (int64_t)p.T * kDqk, p.status);
+            cp_async16(unit + dsto[q][j], s, bytes);
+          }
         }
         cp_async_arrive(bar_addr(sb, KV_FULL + slot));
       }
@@ -961,6 +976,27 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status) {
   __syncthreads();
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status);
 }
+// Bounds-check self-test of the debug build: one gather source and one scatter
+// destination that lie past the logical buffers (the first 16 elements of these
+// arrays) but inside the arrays; both checks must fail, record kErrBounds and skip
+// the access.  Product builds compile an empty kernel (the export refuses to run it).
+__device__ __align__(16) uint16_t g_bounds_buf[64];
+__device__ __align__(16) float g_bounds_fbuf[64];
+__global__ void __launch_bounds__(32) bounds_selftest_kernel(uint32_t* status) {
+#ifdef SMLA_DEBUG
+  __shared__ __align__(16) uint16_t sdst[8];
+  if (threadIdx.x == 0) {
+    const uint16_t* src = g_bounds_buf + 24;
+    uint32_t bytes = 16u;
+    check_src(src, bytes, static_cast<const uint16_t*>(g_bounds_buf), 16, status);
+    cp_async16(smem_u32(sdst), src, bytes);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (check_range(g_bounds_fbuf + 32, 4, static_cast<float*>(g_bounds_fbuf), 16, status)) g_bounds_fbuf[32] = 1.f;
+  }
+#else
+  (void)status;
+#endif
+}
 // exchange scratch of the tensor-core kernels (16 MiB), one slot per SM
 __device__ __align__(256) float g_xchg[kXchgSlots * kXchgSlotFloats];
 
@@ -991,6 +1027,13 @@ cudaError_t launch_wait_selftest(cudaStream_t s) {
   uint32_t* status = tc_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounds_selftest(cudaStream_t s) {
+  uint32_t* status = tc_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  bounds_selftest_kernel<<<1, 32, 0, s>>>(status);
   return cudaGetLastError();
 }
 

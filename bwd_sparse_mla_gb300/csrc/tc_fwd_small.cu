@@ -178,7 +178,8 @@ __device__ __forceinline__ void produce(const SmallFwdParams& p, uint32_t sb, ui
       const uint16_t* qsrc = p.q + ((int64_t)t * p.H + (real ? h : 0)) * kDqk + 8 * c16;
 #pragma unroll
       for (int c = 0; c < 9; ++c)
-        cp_async16(sb + SM_Q + c * kQChunk + h * 128 + ((c16 ^ (h & 7)) << 4), qsrc + 64 * c, real ? 16u : 0u);
+        gather16(sb + SM_Q + c * kQChunk + h * 128 + ((c16 ^ (h & 7)) << 4), qsrc + 64 * c, real ? 16u : 0u, p.q,
+                 (int64_t)p.T * p.H * kDqk, p.status);
       cp_async_arrive(bar_addr(sb, Q_FULL));
     }
     int nxt[R], nm[4] = {-1, -1, -1, -1};
@@ -225,8 +226,8 @@ __device__ __forceinline__ void produce(const SmallFwdParams& p, uint32_t sb, ui
         const uint32_t unit = sb + SM_LAT + slot * kLatBytes;
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-          cp_async16(unit + dsto[j], src[j] + 128 * u, nbytes[j]);
-          cp_async16(unit + 128 * 128 + dsto[j], src[j] + 128 * u + 64, nbytes[j]);
+          gather16(unit + dsto[j], src[j] + 128 * u, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
+          gather16(unit + 128 * 128 + dsto[j], src[j] + 128 * u + 64, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
         }
         cp_async_arrive(bar_addr(sb, LAT_FULL + slot));
       }
@@ -239,7 +240,7 @@ __device__ __forceinline__ void produce(const SmallFwdParams& p, uint32_t sb, ui
           break;
         const uint32_t unit = sb + SM_TAIL + slot * kTailBytes;
 #pragma unroll
-        for (int j = 0; j < R; ++j) cp_async16(unit + dsto[j], src[j] + 512, nbytes[j]);
+        for (int j = 0; j < R; ++j) gather16(unit + dsto[j], src[j] + 512, nbytes[j], p.kv, (int64_t)p.T * kDqk, p.status);
         cp_async_arrive(bar_addr(sb, TAIL_FULL + slot));
       }
       if (warp == 0) {                     // slot validity of the block for the softmax

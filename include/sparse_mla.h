@@ -239,11 +239,14 @@ const char* sparse_mla_last_error(void);
 /* Library version string. */
 const char* sparse_mla_version(void);
 
-/* Reads the status word of the tensor-core kernels on the current device
- * into *status (HOST pointer): 0 = every bounded wait inside those kernels
- * completed; 1 = some wait gave up after its time limit, the kernel returned
- * early and the outputs of that call are not valid.  With clear != 0 the
- * word is reset to 0.  Synchronizes with the device. */
+/* Reads the device status word of the library's kernels on the current
+ * device into *status (HOST pointer): 0 = every bounded wait inside the
+ * tensor-core kernels completed (and, in the debug build, every bounds check
+ * passed); 1 = some wait gave up after its time limit, the kernel returned
+ * early and the outputs of that call are not valid; 2 = (debug build only) a
+ * gathered row or scatter address fell outside its buffer and that access was
+ * skipped, so the outputs are not valid.  The first error is kept.  With
+ * clear != 0 the word is reset to 0.  Synchronizes with the device. */
 int sparse_mla_device_status(uint32_t* status, int clear);
 
 /* Failure-detection self-test (no counterpart in the source pages).  Enqueues
@@ -255,6 +258,17 @@ int sparse_mla_device_status(uint32_t* status, int clear);
  * (sparse_mla_device_status(&s, 1)); until then it also reports 1 for the
  * other kernels.  Returns 0, or -EINVAL / -EIO as the other calls. */
 int sparse_mla_wait_selftest(void* stream);
+
+/* Bounds-check self-test (no counterpart in the source pages; the library's
+ * debug build, compiled with -DSMLA_DEBUG, checks every 16-byte gather source
+ * and every scatter destination against its buffer before the access, records
+ * status 2 on a failure and skips the access, never trapping).  Enqueues on
+ * `stream` one small kernel whose checks probe addresses past a logical buffer
+ * (but inside its allocation): both must fail, so the status word becomes 2
+ * and nothing is read or written there.  Returns 0 in the debug build,
+ * -ENOSYS in the product build (whose checks compile to nothing), or -EINVAL /
+ * -EIO as the other calls. */
+int sparse_mla_bounds_selftest(void* stream);
 
 /* Number of CUDA kernels this process has launched through the library so
  * far (all threads, all devices).  Diagnostics only: benchmarks read it
