@@ -32,6 +32,15 @@ def _with_padding_holes(w, seed):
     return w
 
 
+def _with_empty_run(w, lo, hi):
+    """Rows lo..hi-1 get only padding: every persistent CTA (pair) then meets a run of
+    consecutive all-padding tokens between tokens with valid slots."""
+    idx = w.indices.reshape(w.T, w.topk)
+    idx[lo:hi] = -1
+    w.indices = idx.reshape(w.T, 1, w.topk)
+    return w
+
+
 SMALL = {
     "cfg1-tiny": lambda: W.make_workload(1),
     "ragged-H8": lambda: W.make_custom(1000, 8, 128, [300, 576, 124], seed=11, empty_rows=5),
@@ -46,6 +55,10 @@ SMALL = {
     # top-k above the tensor-core kernels' limit (runs the CUDA-core kernels)
     "bigtopk-H128": lambda: W.make_custom(260, 128, 16448, [260], seed=17, empty_rows=2),
     "bigtopk-H8": lambda: W.make_custom(200, 8, 16448, [200], seed=18, empty_rows=2),
+    # runs of all-padding tokens in every CTA's token list, between tokens with valid slots
+    "empty-run-H128": lambda: _with_empty_run(W.make_custom(1200, 128, 256, [1200], seed=19), 300, 900),
+    "empty-run-H64": lambda: _with_empty_run(W.make_custom(1200, 64, 320, [700, 500], seed=20), 250, 950),
+    "empty-run-H8": lambda: _with_empty_run(W.make_custom(1400, 8, 256, [1400], seed=21), 300, 1100),
 }
 
 
