@@ -728,10 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * mr);
           mbar_arrive(bar_addr(sb, M_EMPTY + mr));
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const uint64_t c2x2 = f32x2(p.c2, p.c2);
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj) {
-            s[jj] = ((mask >> jj) & 1ull) ? s[jj] * p.c2 : -INFINITY;
+          for (int jj = 0; jj < 64; jj += 2) {
+            float a0, a1;
+            f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), a0, a1);
+            s[jj] = ((mask >> jj) & 1ull) ? a0 : -INFINITY;
+            s[jj + 1] = ((mask >> (jj + 1)) & 1ull) ? a1 : -INFINITY;
             mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
+            mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
           }
           const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           // the running state after the token's previous block, from the other group; at
@@ -757,16 +762,23 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             // a listed block has a valid slot, so m_new is finite; the guard keeps
             // exp2(-inf - -inf) out regardless
             const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f}, sbf4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t msub2 = f32x2(m_sub, m_sub);
+            uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)}, sbf2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-              const float p0 = ex2(s[2 * jj] - m_sub), p1 = ex2(s[2 * jj + 1] - m_sub);   // -inf -> 0
-              sum4[jj & 3] += p0 + p1;
+              float a0, a1;
+              f32x2_split(sub_f32x2(f32x2(s[2 * jj], s[2 * jj + 1]), msub2), a0, a1);
+              const float p0 = ex2(a0), p1 = ex2(a1);   // -inf -> 0
+              sum2[jj & 1] = add_f32x2(sum2[jj & 1], f32x2(p0, p1));
               pk[jj] = pack_bf16x2(p0, p1);
-              sbf4[jj & 3] += bf16_lo(pk[jj]) + bf16_hi(pk[jj]);   // the weights the PV MMA actually uses
+              // the weights the PV MMA actually uses
+              sbf2[jj & 1] = add_f32x2(sbf2[jj & 1], f32x2(bf16_lo(pk[jj]), bf16_hi(pk[jj])));
             }
-            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-            l_bf = l_bf * alpha + ((sbf4[0] + sbf4[1]) + (sbf4[2] + sbf4[3]));
+            float u0, u1, u2, u3, w0, w1, w2, w3;
+            f32x2_split(sum2[0], u0, u1); f32x2_split(sum2[1], u2, u3);
+            f32x2_split(sbf2[0], w0, w1); f32x2_split(sbf2[1], w2, w3);
+            l = l * alpha + ((u0 + u1) + (u2 + u3));
+            l_bf = l_bf * alpha + ((w0 + w1) + (w2 + w3));
             m_run = m_new;
           } else {
 #pragma unroll
