@@ -729,14 +729,23 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           mbar_arrive(bar_addr(sb, M_EMPTY + mr));
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           const uint64_t c2x2 = f32x2(p.c2, p.c2);
+          if (mask == ~0ull) {               // no padding in the block (the common case): no selects
 #pragma unroll
-          for (int jj = 0; jj < 64; jj += 2) {
-            float a0, a1;
-            f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), a0, a1);
-            s[jj] = ((mask >> jj) & 1ull) ? a0 : -INFINITY;
-            s[jj + 1] = ((mask >> (jj + 1)) & 1ull) ? a1 : -INFINITY;
-            mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
-            mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
+            for (int jj = 0; jj < 64; jj += 2) {
+              f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), s[jj], s[jj + 1]);
+              mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
+              mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 64; jj += 2) {
+              float a0, a1;
+              f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), a0, a1);
+              s[jj] = ((mask >> jj) & 1ull) ? a0 : -INFINITY;
+              s[jj + 1] = ((mask >> (jj + 1)) & 1ull) ? a1 : -INFINITY;
+              mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
+              mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
+            }
           }
           const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           // the running state after the token's previous block, from the other group; at
