@@ -26,7 +26,8 @@
 //     the O rows whose running max moved, and issues O += P V (M = 128,
 //     N = 256, K = 64, twice).  At the end of a token O is divided by the sum
 //     of the bf16-rounded weights (so the rounding of P cancels in `out`) and
-//     written as bf16; a row with no valid slot is written as exact zeros.
+//     written as bf16; a row with no valid slot is written as exact zeros.  The
+//     sum of the rounded weights is taken here, from each block's P as it arrives.
 //
 // Both CTAs gather with 16-byte cp.async into rings of 128B-swizzled units
 // that flow from one token into the next; a padding slot copies zero bytes
@@ -81,14 +82,13 @@ constexpr int kPBufStride = 17 * 1024;                   // 1024-aligned buffer 
 // score CTA: K ring, P staging, the running state, the mask ring
 constexpr int SM_K = 0;
 constexpr int SM_STG = SM_K + kSRing * kSPairUnit;
-constexpr int SM_STATE = SM_STG + kNS * kPBufStride;     // 128 heads x float4 (m, l, l_bf)
+constexpr int SM_STATE = SM_STG + kNS * kPBufStride;     // 128 heads x float4 (m, l)
 constexpr int SM_MASK = SM_STATE + 128 * 16;             // kMaskRing x u64
 constexpr int kScoreEnd = SM_MASK + 8 * kMaskRing;
 // output CTA: V ring, P buffers, the final sums of two tokens
 constexpr int SM_V = 0;
 constexpr int SM_P = SM_V + kORing * kOUnitCh * kChunkKV;
-constexpr int SM_LBF = SM_P + kNP * kPBufStride;         // 2 x 128 floats from the score CTA
-constexpr int kOutEnd = SM_LBF + 2 * 512;
+constexpr int kOutEnd = SM_P + kNP * kPBufStride;
 // common to both roles: the token ring (block count of the two newest tokens),
 // the producers' per-token block flags and list
 constexpr int SM_TOK = kScoreEnd > kOutEnd ? kScoreEnd : kOutEnd;   // 2 x int
@@ -99,10 +99,10 @@ constexpr int SM_BAR = (SM_NB + 8 + 7) & ~7;
 // barriers: the same slots carry role-specific meanings
 enum ScoreBar { KV_FULL = 0, KV_EMPTY = kSRing, M_FULL = 2 * kSRing, M_EMPTY = M_FULL + kMaskRing,
                 Q_EMPTY = M_EMPTY + kMaskRing, S_FULL, S_FREE = S_FULL + 2, ST_FULL = S_FREE + 2,
-                STG_FULL = ST_FULL + 2, STG_FREE = STG_FULL + kNS, P_FREE = STG_FREE + kNS, L_EMPTY = P_FREE + kNP,
-                TOK_FULL_S = L_EMPTY + 2, TOK_EMPTY_S = TOK_FULL_S + 2, NBAR_S = TOK_EMPTY_S + 2 };
+                STG_FULL = ST_FULL + 2, STG_FREE = STG_FULL + kNS, P_FREE = STG_FREE + kNS,
+                TOK_FULL_S = P_FREE + kNP, TOK_EMPTY_S = TOK_FULL_S + 2, NBAR_S = TOK_EMPTY_S + 2 };
 enum OutBar { V_FULL = 0, V_EMPTY = kORing, P_FULL = 2 * kORing, R_DONE = P_FULL + kNP, PV_DONE = R_DONE + kNP,
-              L_FULL = PV_DONE + kNP, O_FREE = L_FULL + 2, TOK_FULL_O, TOK_EMPTY_O = TOK_FULL_O + 2,
+              RS_DONE = PV_DONE + kNP, O_FREE = RS_DONE + kNP, TOK_FULL_O, TOK_EMPTY_O = TOK_FULL_O + 2,
               NBAR_O = TOK_EMPTY_O + 2 };
 constexpr int kNBar = 56;
 static_assert(NBAR_S <= kNBar && NBAR_O <= kNBar, "barrier slots");
@@ -136,9 +136,6 @@ struct TcFwdParams {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8 * i; }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
-}
 // bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
 // another CTA's (addresses from mapa); completes tx on the destination's barrier
 __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
@@ -537,7 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         mbar_init(bar_addr(sb, S_FULL + g), 1);
         mbar_init(bar_addr(sb, S_FREE + g), 128);
         mbar_init(bar_addr(sb, ST_FULL + g), 128);    // group g wrote the running state after its block
-        mbar_init(bar_addr(sb, L_EMPTY + g), 128);    // the output CTA read a token's final sums
         mbar_init(bar_addr(sb, TOK_FULL_S + g), 1);
         mbar_init(bar_addr(sb, TOK_EMPTY_S + g), 1 + 1 + 256);   // MMA, P mover, both softmax groups
       }
@@ -555,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         mbar_init(bar_addr(sb, P_FULL + k), 1);       // armed with expect_tx; the bulk copy completes it
         mbar_init(bar_addr(sb, R_DONE + k), 128);     // rows rescaled where the max moved
         mbar_init(bar_addr(sb, PV_DONE + k), 1);
+        mbar_init(bar_addr(sb, RS_DONE + k), 128);    // the rows summed the block's weights
       }
       for (int g = 0; g < 2; ++g) {
-        mbar_init(bar_addr(sb, L_FULL + g), 128);
         mbar_init(bar_addr(sb, TOK_FULL_O + g), 1);
         mbar_init(bar_addr(sb, TOK_EMPTY_O + g), 1 + 1 + 128);   // MMA, P keeper, rows
       }
@@ -691,7 +687,6 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
       const bool real = kAllHeads || h < p.H;
       volatile float* state = reinterpret_cast<volatile float*>(smem + SM_STATE) + 4 * h;
-      const uint32_t lbf_peer = mapa(sb + SM_LBF + 4 * h, peer), lfull_peer = mapa(bar_addr(sb, L_FULL), peer);
       if (real && ntok > 0) {                  // the first token's q row into L2
         const uint8_t* q0 = reinterpret_cast<const uint8_t*>(p.q + ((int64_t)(p.t0 + cl) * p.H + h) * kDqk);
         for (int c = g; c < 9; c += 2) prefetch_l2(q0 + 128 * c);
@@ -706,9 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q + ((int64_t)(t + ncl) * p.H + h) * kDqk);
           for (int c = g; c < 9; c += 2) prefetch_l2(qn + 128 * c);
         }
-        // l: sum of the fp32 exponentials (gives the LSE); l_bf: sum of the bf16-rounded
-        // weights fed to the PV MMA (normalises O, so the rounding of P cancels in out)
-        float m_run = -INFINITY, l = 0.f, l_bf = 0.f;
+        // l: sum of the fp32 exponentials (gives the LSE); the output CTA sums the
+        // bf16-rounded weights itself
+        float m_run = -INFINITY, l = 0.f;
         const int gb0 = gb;
         for (int j = (g - gb0) & 1; j < nb; j += 2) {
           const int gbj = gb0 + j;
@@ -756,9 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
                                                        abort_flag, p.status))))
             break;
           if (j >= 1) {
-            m_run = state[0]; l = state[1]; l_bf = state[2];
+            m_run = state[0]; l = state[1];
           } else {
-            m_run = -INFINITY; l = 0.f; l_bf = 0.f;
+            m_run = -INFINITY; l = 0.f;
           }
           if (h == 0) SMLA_STAMP(gbj - kTraceGb0, 4);
           float alpha = 1.f;
@@ -772,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             // exp2(-inf - -inf) out regardless
             const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
             const uint64_t msub2 = f32x2(m_sub, m_sub);
-            uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)}, sbf2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+            uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               float a0, a1;
@@ -780,20 +775,16 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
               const float p0 = ex2(a0), p1 = ex2(a1);   // -inf -> 0
               sum2[jj & 1] = add_f32x2(sum2[jj & 1], f32x2(p0, p1));
               pk[jj] = pack_bf16x2(p0, p1);
-              // the weights the PV MMA actually uses
-              sbf2[jj & 1] = add_f32x2(sbf2[jj & 1], f32x2(bf16_lo(pk[jj]), bf16_hi(pk[jj])));
             }
-            float u0, u1, u2, u3, w0, w1, w2, w3;
+            float u0, u1, u2, u3;
             f32x2_split(sum2[0], u0, u1); f32x2_split(sum2[1], u2, u3);
-            f32x2_split(sbf2[0], w0, w1); f32x2_split(sbf2[1], w2, w3);
             l = l * alpha + ((u0 + u1) + (u2 + u3));
-            l_bf = l_bf * alpha + ((w0 + w1) + (w2 + w3));
             m_run = m_new;
           } else {
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) pk[jj] = 0u;   // rows past H: P = 0, O stays 0
           }
-          state[0] = m_run; state[1] = l; state[2] = l_bf;
+          state[0] = m_run; state[1] = l;
           mbar_arrive(bar_addr(sb, ST_FULL + g));
           // P and alpha into a staging buffer (the P mover copies it to the output CTA)
           const int sg = gbj % kNS;
@@ -814,15 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
         gb = gb0 + nb;
         // the group that took the token's last block holds its final state
         const bool last = (nb == 0) ? (g == 0) : (g == ((gb - 1) & 1));
-        if (last) {
-          if (k >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, L_EMPTY + (k & 1)), ((k >> 1) - 1) & 1,
-                                                                     abort_flag, p.status))))
-            break;
-          // the sum of rounded weights goes to the output CTA, the LSE to global memory
-          st_cluster_f32(lbf_peer + 512 * (k & 1), l_bf);
-          mbar_arrive_remote(lfull_peer + 8 * (k & 1));
-          if (real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
-        }
+        if (last && real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : kLseEmpty;
       }
     }
   } else {
@@ -870,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
     } else if (warp == kAuxWarp) {
       if (lane == 0) {
         // P buffer keeper (a warp of its own, like the P mover): arms each buffer for its next block's bulk copy and tells the
-        // score CTA when PV has finished reading it
+        // score CTA when PV and the rows' sums have finished reading it
         const uint32_t pfree_peer = mapa(bar_addr(sb, P_FREE), peer);
         for (int b = 0; b < kNP; ++b) mbar_arrive_expect_tx(bar_addr(sb, P_FULL + b), kPXBytes);
         int gb = 0;
@@ -881,6 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int pb = gb % kNP;
             if (!(ok = mbar_wait(bar_addr(sb, PV_DONE + pb), (gb / kNP) & 1, abort_flag, p.status))) break;
+            if (!(ok = mbar_wait(bar_addr(sb, RS_DONE + pb), (gb / kNP) & 1, abort_flag, p.status))) break;
             mbar_arrive_expect_tx(bar_addr(sb, P_FULL + pb), kPXBytes);   // for block gb + kNP
             mbar_arrive_remote(pfree_peer + 8 * pb);
           }
@@ -893,13 +877,15 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
       const int h = 32 * q4 + lane;
       const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
       const bool real = kAllHeads || h < p.H;
-      const uint32_t lempty_peer = mapa(bar_addr(sb, L_EMPTY), peer);
       int gb = 0;
       bool ok = true;
       for (int k = 0; ok && k < ntok; ++k) {
         const int t = p.t0 + cl + k * ncl;
         const int nb = read_token<true>(p, sb, smem, k, TOK_FULL_O, TOK_EMPTY_O, abort_flag);
         if (!(ok = nb >= 0)) break;
+        // l_bf: sum of the bf16-rounded weights the PV MMA multiplies (normalises O, so the
+        // rounding of P cancels in out), rescaled with O
+        float l_bf = 0.f;
         for (int j = 0; ok && j < nb; ++j, ++gb) {
           const int pb = gb % kNP;
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, P_FULL + pb), (gb / kNP) & 1, abort_flag, p.status))))
@@ -927,14 +913,26 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           }
           tc_fence_before();
           mbar_arrive(bar_addr(sb, R_DONE + pb));
+          {                                      // this head's sum of the block's weights, off the PV path
+            const uint4* prow = reinterpret_cast<const uint4*>(smem + SM_P + pb * kPBufStride + h * 128);
+            uint64_t acc2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = prow[c];
+              acc2[0] = add_f32x2(acc2[0], f32x2(bf16_lo(v.x), bf16_hi(v.x)));
+              acc2[1] = add_f32x2(acc2[1], f32x2(bf16_lo(v.y), bf16_hi(v.y)));
+              acc2[0] = add_f32x2(acc2[0], f32x2(bf16_lo(v.z), bf16_hi(v.z)));
+              acc2[1] = add_f32x2(acc2[1], f32x2(bf16_lo(v.w), bf16_hi(v.w)));
+            }
+            float a0, a1, a2, a3;
+            f32x2_split(acc2[0], a0, a1);
+            f32x2_split(acc2[1], a2, a3);
+            l_bf = l_bf * alpha + ((a0 + a1) + (a2 + a3));
+          }
+          mbar_arrive(bar_addr(sb, RS_DONE + pb));
         }
         if (!ok) break;
-        // epilogue of the token: the final sums, then O once its last PV completed
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_addr(sb, L_FULL + (k & 1)), (k >> 1) & 1, abort_flag,
-                                                           p.status))))
-          break;
-        const float l_bf = reinterpret_cast<volatile float*>(smem + SM_LBF + 512 * (k & 1))[h];
-        mbar_arrive_remote(lempty_peer + 8 * (k & 1));
+        // epilogue of the token: O once its last PV completed
         if (nb > 0 &&
             !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, PV_DONE + (gb - 1) % kNP), ((gb - 1) / kNP) & 1,
                                                      abort_flag, p.status))))
@@ -1001,8 +999,10 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status) {
 // destination that lie past the logical buffers (the first 16 elements of these
 // arrays) but inside the arrays; both checks must fail, record kErrBounds and skip
 // the access.  Product builds compile an empty kernel (the export refuses to run it).
+#ifdef SMLA_DEBUG
 __device__ __align__(16) uint16_t g_bounds_buf[64];
 __device__ __align__(16) float g_bounds_fbuf[64];
+#endif
 __global__ void __launch_bounds__(32) bounds_selftest_kernel(uint32_t* status) {
 #ifdef SMLA_DEBUG
   __shared__ __align__(16) uint16_t sdst[8];
