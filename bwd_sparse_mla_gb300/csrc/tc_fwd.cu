@@ -445,14 +445,16 @@ __device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb,
           nbytes[q][j] = v ? 16u : 0u;
         }
       if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 9);
+      int slot = n % kSRing, lap = n / kSRing;   // kept incrementally over the pair's units
 #pragma unroll 1
       for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
-        const int slot = n % kSRing;
-        if (n >= kSRing &&
-            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + slot), ((n / kSRing) - 1) & 1, abort_flag,
+        if (lap > 0 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(sb, KV_EMPTY + slot), (lap - 1) & 1, abort_flag,
                                                      p.status))))
           break;                           // warp-uniform exit
         const uint32_t unit = sb + SM_K + slot * kSPairUnit;
+        const int fslot = slot;
+        if (++slot == kSRing) { slot = 0; ++lap; }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           if (q == 1 && npair < 2) break;
@@ -464,7 +466,7 @@ __device__ __forceinline__ void produce_score(const TcFwdParams& p, uint32_t sb,
             cp_async16(unit + dsto[q][j], s, bytes);
           }
         }
-        cp_async_arrive(bar_addr(sb, KV_FULL + slot));
+        cp_async_arrive(bar_addr(sb, KV_FULL + fslot));
       }
       if (!ok) break;
       if (pt == 0) SMLA_STAMP(gb - kTraceGb0, 10);
@@ -617,10 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             if (!ok) break;
             SMLA_STAMP(gb - kTraceGb0, 0);
             const int b1 = gb & 1;               // a single block: its buffer and half of the unit
+            int slot = n % kSRing, lap = n / kSRing;   // kept incrementally over the pair's units
 #pragma unroll 1
             for (int c = 0; c < kSUnitsPerPair; ++c, ++n) {
-              const int slot = n % kSRing;
-              if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), (n / kSRing) & 1, abort_flag, p.status))) break;
+              if (!(ok = mbar_wait(bar_addr(sb, KV_FULL + slot), lap & 1, abort_flag, p.status))) break;
               if (c == 0 || c == 3 || c == 6 || c == 8) SMLA_STAMP(gb - kTraceGb0, c == 0 ? 2 : c == 3 ? 6 : c == 6 ? 7 : 8);
               fence_proxy_async_smem();   // cp.async wrote the unit through the generic proxy
               tc_fence_after();
@@ -637,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
                               sdesc_add(dk0, slot * kSPairUnit + b1 * kChunkKV + ks * 32), idesc_s1, (c | ks) != 0);
               }
               mma_commit(bar_addr(sb, KV_EMPTY + slot));
+              if (++slot == kSRing) { slot = 0; ++lap; }
             }
             if (!ok) break;
             mma_commit(bar_addr(sb, S_FULL + (gb & 1)));
