@@ -265,19 +265,37 @@ __device__ __forceinline__ void produce(const SmallFwdParams& p, uint32_t sb, ui
   }
 }
 
-template <int N>
-__device__ __forceinline__ void warp_max(float (&v)[N]) {
+// One step of a transposed warp reduction: lanes whose bit o is set keep the upper
+// HALF of their values and send the lower half, the others the reverse; HALF == 0
+// is a plain butterfly on the single remaining value.
+template <int HALF, bool kMax>
+__device__ __forceinline__ void wrt_step(float* v, int lane, int o) {
+  if constexpr (HALF == 0) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], o);
+    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+  } else {
+    const bool up = (lane & o) != 0;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = fmaxf(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
+    for (int i = 0; i < HALF; ++i) {
+      const float send = up ? v[i] : v[i + HALF];
+      const float keep = up ? v[i + HALF] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
 }
-template <int N>
-__device__ __forceinline__ void warp_sum(float (&v)[N]) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+// Transposed warp reduction of N values per lane (N = 16 or 32): N - 1 (+ 1) shuffles
+// instead of 5 N.  Returns, in lane L, the reduction over the warp of value index
+// L >> (5 - log2 N).
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_t(float (&v)[N], int lane) {
+  static_assert(N == 16 || N == 32, "value count");
+  wrt_step<(N >> 1), kMax>(v, lane, 16);
+  wrt_step<(N >> 2), kMax>(v, lane, 8);
+  wrt_step<(N >> 3), kMax>(v, lane, 4);
+  wrt_step<(N >> 4), kMax>(v, lane, 2);
+  wrt_step<(N >> 5), kMax>(v, lane, 1);
+  return v[0];
 }
 
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_small_kernel(SmallFwdParams p) {
@@ -442,13 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_small_kernel(SmallFwdParam
           s[h] = valid ? s[h] * p.c2 : -INFINITY;
           mx[h] = s[h];
         }
-        warp_max(mx);
-        if (lane < kHN) {
-          float v = mx[0];
-#pragma unroll
-          for (int h = 1; h < kHN; ++h) v = lane == h ? mx[h] : v;
-          rmax[ws * kHN + lane] = v;
-        }
+        static_assert(kHN == 16, "lane L holds head L >> 1 after the transposed reduction");
+        const float mxl = warp_reduce_t<kHN, true>(mx, lane);
+        if ((lane & 1) == 0) rmax[ws * kHN + (lane >> 1)] = mxl;
         named_bar_sync(kSmBar, 128);
         float alpha[kHN], msub[kHN];
         bool moved = false;
@@ -473,13 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_small_kernel(SmallFwdParam
           ps[h] = pv;
           ps[kHN + h] = bf16_lo(pk);                    // the weight the PV MMA actually uses
         }
-        warp_sum(ps);
-        if (lane < 2 * kHN) {
-          float v = ps[0];
-#pragma unroll
-          for (int h = 1; h < 2 * kHN; ++h) v = lane == h ? ps[h] : v;
-          rsum[ws * 2 * kHN + lane] = v;
-        }
+        rsum[ws * 2 * kHN + lane] = warp_reduce_t<2 * kHN, false>(ps, lane);   // lane L: value L
         named_bar_sync(kSmBar, 128);
 #pragma unroll
         for (int h = 0; h < kHN; ++h) {
