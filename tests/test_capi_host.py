@@ -177,3 +177,17 @@ def test_dkv_cast_checks(lib):
     assert lib.sparse_mla_dkv_cast(None, FAKE, 4, None) == EINVAL
     assert lib.sparse_mla_dkv_cast(FAKE, MISALIGNED, 4, None) == EINVAL
     assert lib.sparse_mla_dkv_cast(None, None, 0, None) == 0
+
+
+def test_bounds_selftest_is_refused_in_the_product_build(lib):
+    # the product build compiles the device bounds checks away, so it has nothing to test
+    assert lib.sparse_mla_bounds_selftest(None) == -38        # -ENOSYS
+    assert "debug build" in capi.sparse_mla_last_error()
+
+
+def test_debug_build_compiles_and_exports_every_declared_symbol(tmp_path):
+    lib_path = str(tmp_path / "libsparse_mla_debug.so")
+    B.build(["-DSMLA_DEBUG"], lib=lib_path, obj=str(tmp_path / "obj"))
+    dbg = ctypes.CDLL(lib_path)
+    for s in declared_symbols():
+        assert hasattr(dbg, s), s
