@@ -726,26 +726,19 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
           const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + SM_MASK + 8 * mr);
           mbar_arrive(bar_addr(sb, M_EMPTY + mr));
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          const uint64_t c2x2 = f32x2(p.c2, p.c2);
+          // the scale (c2 > 0) is applied to the block max here and folded into the exponent
+          // below, so the raw scores are only masked
           if (mask == ~0ull) {               // no padding in the block (the common case): no selects
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 2) {
-              f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), s[jj], s[jj + 1]);
-              mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
-              mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
-            }
+            for (int jj = 0; jj < 64; ++jj) mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
           } else {
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 2) {
-              float a0, a1;
-              f32x2_split(mul_f32x2(f32x2(s[jj], s[jj + 1]), c2x2), a0, a1);
-              s[jj] = ((mask >> jj) & 1ull) ? a0 : -INFINITY;
-              s[jj + 1] = ((mask >> (jj + 1)) & 1ull) ? a1 : -INFINITY;
+            for (int jj = 0; jj < 64; ++jj) {
+              s[jj] = ((mask >> jj) & 1ull) ? s[jj] : -INFINITY;
               mx4[jj & 3] = fmaxf(mx4[jj & 3], s[jj]);
-              mx4[(jj + 1) & 3] = fmaxf(mx4[(jj + 1) & 3], s[jj + 1]);
             }
           }
-          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.c2;
           // the running state after the token's previous block, from the other group; at
           // a token's first block the state starts afresh, but the wait still orders this
           // group's write of the shared state after the other group's last one
@@ -769,12 +762,12 @@ __global__ void __launch_bounds__(kThreads, 1) __cluster_dims__(2, 1, 1)
             // a listed block has a valid slot, so m_new is finite; the guard keeps
             // exp2(-inf - -inf) out regardless
             const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-            const uint64_t msub2 = f32x2(m_sub, m_sub);
+            const uint64_t c2x2 = f32x2(p.c2, p.c2), nmsub2 = f32x2(-m_sub, -m_sub);
             uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               float a0, a1;
-              f32x2_split(sub_f32x2(f32x2(s[2 * jj], s[2 * jj + 1]), msub2), a0, a1);
+              f32x2_split(fma_f32x2(f32x2(s[2 * jj], s[2 * jj + 1]), c2x2, nmsub2), a0, a1);   // S c2 - m
               const float p0 = ex2(a0), p1 = ex2(a1);   // -inf -> 0
               sum2[jj & 1] = add_f32x2(sum2[jj & 1], f32x2(p0, p1));
               pk[jj] = pack_bf16x2(p0, p1);
