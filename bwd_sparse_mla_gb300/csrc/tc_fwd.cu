@@ -9,8 +9,9 @@
 //     dims, bf16) in TMEM as the A operand and gathers the full 576-wide KV
 //     rows named by each block of 64 top-k slots.  q itself arrives through
 //     the same ring of units as the KV rows (nine 64-dim chunks ahead of the
-//     token's first block) and is copied into TMEM by the tensor pipe.  Per block it computes the
-//     complete scores S = q K^T (M = 128 heads, N = 64 slots, K = 576).  Two
+//     token's first block) and is copied into TMEM by the tensor pipe.  It
+//     computes the complete scores S = q K^T of two blocks at a time
+//     (M = 128 heads, N = 2 x 64 slots, K = 576).  Two
 //     softmax groups (one thread per head each) take alternate blocks: padding
 //     slots are masked to -inf, the running max moves lazily (only when a
 //     block max exceeds it by more than 8 in the log2 domain) and passes from
