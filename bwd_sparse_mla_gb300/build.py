@@ -65,4 +65,6 @@ def debug_paths() -> tuple:
 
 
 if __name__ == "__main__":
-    print(build(sys.argv[1:]))
+    flags = sys.argv[1:]
+    # the bounds-checked debug build never replaces the product library
+    print(build(flags, *debug_paths()) if "-DSMLA_DEBUG" in flags else build(flags))
