@@ -17,6 +17,7 @@ pairs keep it two orders of magnitude inside.  This is why the kernels carry
 the pairs.
 """
 import numpy as np
+import pytest
 
 import oracle.sparse_mla_ref as orc
 from bwd_sparse_mla_gb300 import workloads as W
@@ -64,14 +65,18 @@ def model_bwd(w, out_in, lse_in, roundings):
     return res
 
 
-def test_bf16_pairs_are_needed_for_the_max_abs_bound():
-    # ragged H = 128 case at the headline's q scale, with empty rows
+@pytest.fixture(scope="module")
+def case():
+    """Ragged H = 128 case at the headline's q scale, with empty rows; the exact
+    forward and what the backward is given (bf16 out, fp32 lse)."""
     w = W.make_custom(520, 128, 320, [8, 200, 312], seed=15, empty_rows=3, q_std=8.0)
-    q = orc.bf16_bits_to_f64(w.q)
     out, lse = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale)
-    # what the backward is given: bf16 out and fp32 lse
-    out_in = bf16_round(out)
-    lse_in = lse.astype(np.float32).astype(np.float64)
+    return w, out, lse, bf16_round(out), lse.astype(np.float32).astype(np.float64)
+
+
+def test_bf16_pairs_are_needed_for_the_max_abs_bound(case):
+    w, _, _, out_in, lse_in = case
+    q = orc.bf16_bits_to_f64(w.q)
     dq_ref, dkv_ref = orc.sparse_mla_bwd(w.q, w.kv, out_in, w.dout, lse_in, w.indices, w.scale)
 
     res = model_bwd(w, out_in, lse_in, {"exact": None, "bf16": bf16_round, "pair": bf16_pair})
@@ -100,3 +105,20 @@ def test_bf16_pairs_are_needed_for_the_max_abs_bound():
     assert dkv_abs < 2e-3, dkv_abs
     assert dkv_rel < 1e-5, dkv_rel
     assert np.all(np.abs(dq_out - dq_ref) <= abs_bound(dq_ref, "bf16"))
+
+
+def test_bf16_out_alone_moves_the_exact_gradients_past_the_bound(case):
+    """The backward takes out as given (the kernel call of slime issue #2201,
+    "Strongest repro evidence"); out is bf16 at the interface.  Rounding the exact
+    out to bf16 moves Delta = rowsum(dO * out), and with it the exact dkv, by more
+    than 2e-2 where a kv row is named by hundreds of queries.  So no bf16
+    interface can be compared with the oracle chain fed its own fp64 out: the
+    chained GPU test compares the GPU backward with the oracle backward given the
+    GPU forward's own bf16 out and fp32 lse."""
+    w, out, lse, out_in, lse_in = case
+    dq_a, dkv_a = orc.sparse_mla_bwd(w.q, w.kv, out, w.dout, lse, w.indices, w.scale)
+    dq_b, dkv_b = orc.sparse_mla_bwd(w.q, w.kv, out_in, w.dout, lse_in, w.indices, w.scale)
+    assert np.abs(dkv_b - dkv_a).max() > MAX_ABS
+    # the change comes from the rounding of out: fp32 lse alone moves dkv far less
+    _, dkv_c = orc.sparse_mla_bwd(w.q, w.kv, out, w.dout, lse_in, w.indices, w.scale)
+    assert np.abs(dkv_c - dkv_a).max() < 0.1 * np.abs(dkv_b - dkv_a).max()
