@@ -20,10 +20,10 @@ that output grows when the inputs grow by c:
   kv rows scaled by c (c = 256): scores, LSE, out (P V) and dkv grow by c, and
   dq = dS K by c^2, because dS = P (dP - Delta) carries dP = dO V (factor c)
   and K brings another.
-A CPU simulation of the kernel's rounding (fp32 P, dP and Delta; dS' as bf16
-hi + lo) on the scaled-kv case gives a dq error of about 500 where two
-dominant rows cancel, against terms of 2.6e5: the fp32 arithmetic itself, not
-the kernel, sets that figure."""
+On the scaled-kv case the dq error is about 500: dq reaches 2.6e5, where half
+a bf16 step is 512, so its bf16 output rounding alone accounts for it (a CPU
+model of the kernel's arithmetic is within about 1e-5 of the exact dq before
+that rounding)."""
 import numpy as np
 import pytest
 import torch

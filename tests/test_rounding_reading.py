@@ -21,7 +21,7 @@ import pytest
 
 import oracle.sparse_mla_ref as orc
 from bwd_sparse_mla_gb300 import workloads as W
-from tests.gpu_helpers import MAX_ABS, abs_bound
+from tests.gpu_helpers import MAX_ABS, abs_bound, half_step_bf16
 
 D_LATENT = 512
 
@@ -122,3 +122,45 @@ def test_bf16_out_alone_moves_the_exact_gradients_past_the_bound(case):
     # the change comes from the rounding of out: fp32 lse alone moves dkv far less
     _, dkv_c = orc.sparse_mla_bwd(w.q, w.kv, out, w.dout, lse_in, w.indices, w.scale)
     assert np.abs(dkv_c - dkv_a).max() < 0.1 * np.abs(dkv_b - dkv_a).max()
+
+
+def test_large_kv_rows_dq_error_is_its_bf16_output_rounding():
+    """Ten kv rows scaled by 256 (the finite-domain case of the GPU tests): dq
+    grows to about 2.6e5, where half a bf16 step is 512.  A model of the
+    kernels' arithmetic (fp32 P, dP and Delta; dS' in fp32 and then as a bf16
+    pair) stays within about 1e-5 of the exact dq before dq is rounded to its
+    bf16 output; after that rounding its error is a few hundred, all of it the
+    output's half step."""
+    w = W.make_custom(300, 16, 256, [300], seed=92, empty_rows=2)
+    kv = orc.bf16_bits_to_f64(w.kv).reshape(w.T, -1)
+    rows = np.random.default_rng(5).choice(w.T, 10, replace=False)
+    kv[rows] *= 256.0                                    # exact in bf16
+    w.kv = W.f32_to_bf16_bits(kv.astype(np.float32)).reshape(w.T, 1, -1)
+    q = orc.bf16_bits_to_f64(w.q)
+    do = orc.bf16_bits_to_f64(w.dout)
+    out, lse = orc.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale)
+    out_in, lse_in = bf16_round(out), lse.astype(np.float32).astype(np.float64)
+    dq_ref, _ = orc.sparse_mla_bwd(w.q, w.kv, out_in, w.dout, lse_in, w.indices, w.scale)
+
+    f32 = np.float32
+    log2e = f32(np.log2(np.e))
+    c2 = f32(w.scale) * log2e                            # score scale in the exp2 domain
+    idx = w.indices.reshape(w.T, -1)
+    dq = np.zeros_like(dq_ref)
+    for t in range(w.T):
+        J = orc.valid_slots(idx[t], w.T)
+        if J.size == 0:
+            continue
+        K = kv[J]
+        s = (q[t] @ K.T).astype(f32)                     # fp32 scores (unscaled)
+        P = np.exp2(s * c2 - (lse_in[t].astype(f32) * log2e)[:, None])
+        dP = (do[t] @ K[:, :D_LATENT].T).astype(f32)
+        dl = (do[t] * out_in[t]).sum(axis=1).astype(f32)
+        dSp = (f32(w.scale) * P * (dP - dl[:, None])).astype(np.float64)
+        dq[t] = bf16_pair(dSp) @ K
+    big = np.abs(dq_ref).max()
+    assert big > 2e5
+    assert np.abs(dq - dq_ref).max() < 2e-5 * big        # before the output rounding
+    err = np.abs(bf16_round(dq) - dq_ref)
+    assert err.max() > 100.0                             # the figure the GPU shows (about 500)
+    assert np.all(err <= half_step_bf16(dq_ref) + 2e-5 * big)
